@@ -1,0 +1,152 @@
+/*
+ * jfa.h -- C ABI of libjfa, jagged FlashAttention forward and backward for
+ * GB300 (sm_103a).
+ *
+ * The operation (jagged FlashAttention pages: the alphasignal news page,
+ * "GEM's sequences do not fit a fixed grid"; the PyTorch-blog summary, "JFA
+ * efficiently handles jagged sequences by applying FlashAttention directly
+ * to packed Q/K/V tensors and offsets"): B variable-length sequences are
+ * packed back to back, with no padding, and addressed by an offsets array;
+ * for every sequence b and head h
+ *
+ *     O_b = softmax(scale * Q_b K_b^T) V_b,   LSE_b = logsumexp(scale * Q_b K_b^T)
+ *
+ * row by row, with no mask inside a sequence.  In broadcast mode one dense
+ * query block Q [Lq, H, D] attends to every sequence (same page: "GEM also
+ * broadcasts one dense query across every sequence in a batch") and the
+ * backward sums dQ over the batch.
+ *
+ * Layouts (all row-major, contiguous):
+ *   K, V        bf16 [kv_offsets[B], H, D]
+ *   Q           bf16 [q_offsets[B], H, D]            (self mode)
+ *               bf16 [Lq, H, D]                      (broadcast mode)
+ *   O, dO       bf16 [n_o, H, D], n_o = q_offsets[B] (self) or B*Lq (broadcast, b-major)
+ *   LSE         fp32 [H, n_o], natural log of the row sum, scale included;
+ *               -inf for rows of a sequence with no keys
+ *   dQ          fp32, the shape of Q (broadcast: summed over all sequences)
+ *   dK, dV      bf16, the shape of K
+ * bf16 is IEEE-754 binary16-brain (8-bit exponent), passed as raw 16-bit
+ * words.  Supported: D in {64, 128}; every device pointer 16-byte aligned.
+ *
+ * Ownership: the caller owns every tensor and the stream.  A plan owns a
+ * small device copy of the offsets and of the tile schedule; it must outlive
+ * the stream work that uses it.  jfa_fwd / jfa_bwd allocate nothing and are
+ * asynchronous on the given stream (a cudaStream_t passed as void*; NULL is
+ * the legacy default stream).
+ *
+ * Errors: every entry point returns a jfa_status; nothing throws across the
+ * ABI.  Argument problems are reported before anything is launched.  Device
+ * waits in the kernels are bounded: a wait that runs out records
+ * JFA_ERR_DEVICE_TIMEOUT in the plan's device status word, which
+ * jfa_plan_device_status reads back.
+ */
+#ifndef JFA_H
+#define JFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum jfa_status {
+  JFA_OK = 0,
+  JFA_ERR_INVALID_ARG = 1,    /* null pointer, non-positive size, bad direction ... */
+  JFA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128}, no sm_100-family GPU */
+  JFA_ERR_BAD_OFFSETS = 3,    /* offsets[0] != 0, decreasing, or total >= 2^31 */
+  JFA_ERR_ALIGNMENT = 4,      /* a device pointer is not 16-byte aligned */
+  JFA_ERR_WORKSPACE = 5,      /* workspace missing or smaller than jfa_bwd_workspace_bytes */
+  JFA_ERR_CUDA = 6,           /* a CUDA runtime call failed */
+  JFA_ERR_DEVICE_TIMEOUT = 7  /* a kernel wait ran out (see jfa_plan_device_status) */
+} jfa_status;
+
+/* Tile geometry: query rows per forward tile and key rows per backward tile. */
+#define JFA_BLOCK_M 128
+#define JFA_BLOCK_N 128
+
+typedef struct jfa_plan* jfa_plan_t;
+
+/*
+ * Build a plan for one batch shape.
+ *   kv_offsets_host  int32 [B+1], host memory: kv_offsets[0] = 0, non-decreasing.
+ *   q_offsets_host   int32 [B+1] host offsets of the queries (self mode; may
+ *                    equal kv_offsets), or NULL for broadcast mode.
+ *   B, H             sequences and heads (B >= 1, H >= 1).
+ *   Lq               broadcast mode: rows of the dense Q (>= 0); ignored in self mode.
+ *   D                head dimension, 64 or 128.
+ *   num_ctas         persistent CTAs per launch; 0 = one per SM of the current device.
+ *   stream           stream for the host-to-device upload of offsets and tiles.
+ * The tile schedule follows the pages' description: forward tiles
+ * (b, h, query block) are sorted by key/value workload and dealt to the CTAs
+ * in zigzag (boustrophedon) order (alphasignal page, "Five changes unlocked
+ * the gains", item 1); backward tiles (b, h, key block) exist only where the
+ * sequence has queries and are dealt round-robin (yuxiaoba note, "Why both
+ * static and dynamic balancing help").  On success *out receives the plan.
+ * Allocates device memory; the host arrays are not retained.
+ */
+int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                    int Lq, int D, int num_ctas, void* stream, jfa_plan_t* out);
+
+/* Release a plan (synchronises the device first so in-flight work finishes). */
+int jfa_plan_destroy(jfa_plan_t plan);
+
+/*
+ * Copy a plan's tile schedule to host memory.  dir: 0 forward, 1 backward.
+ * tiles_host receives T records of four int32 {b, h, block, cost} grouped by
+ * CTA, cta_ptr_host receives P+1 CSR offsets (P = min(num_ctas, T)).  Either
+ * buffer may be NULL to query only *T and *P.  Buffers must hold 4*T and P+1
+ * int32.
+ */
+int jfa_plan_tiles(jfa_plan_t plan, int dir, int32_t* tiles_host, int32_t* cta_ptr_host, int* T,
+                   int* P);
+
+/*
+ * Host-only schedule builder (no GPU needed): the same lists a plan holds,
+ * from host lengths.  q_lengths == NULL means broadcast with Lq rows.  Call
+ * once with tiles_out == NULL to learn *T and *P, then with buffers of 4*T
+ * and P+1 int32.
+ */
+int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                    int Lq, int num_ctas, int dir, int32_t* tiles_out, int32_t* cta_ptr_out, int* T,
+                    int* P);
+
+/*
+ * Forward: out = softmax(scale Q K^T) V per sequence and head, lse as above.
+ * q, k, v, out: bf16 device tensors in the layouts above; lse: fp32 device.
+ * Rows of sequences without keys get O = 0 and LSE = -inf.
+ */
+int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float scale, void* out,
+            float* lse, void* stream);
+
+/* Bytes of device workspace jfa_bwd needs (the fp32 row sums Delta = rowsum(dO * O)). */
+size_t jfa_bwd_workspace_bytes(jfa_plan_t plan);
+
+/*
+ * Backward of jfa_fwd.  Inputs q, k, v, out (the forward's O), dout (dO), lse
+ * (the forward's LSE) and the forward's scale.  Outputs dq (fp32, overwritten -- the library clears it
+ * on the stream), dk and dv (bf16).  workspace: device memory of at least
+ * jfa_bwd_workspace_bytes(plan) bytes, 16-byte aligned.  The backward first
+ * forms Delta_i = sum_d dO_id O_id (the row sum the TLX Block Attention page
+ * calls the "Di" preprocessing, "One Constraint, Five Eliminations"), then
+ * runs the key/value-stationary pass that produces dK, dV and reduce-adds dQ.
+ */
+int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const void* out,
+            const void* dout, const float* lse, float scale, float* dq, void* dk, void* dv,
+            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Read the plan's device status word (synchronises `stream`), then clear it.
+ * Returns JFA_ERR_DEVICE_TIMEOUT when a kernel recorded a wait that ran out,
+ * JFA_OK otherwise; *raw (optional) receives the raw word.
+ */
+int jfa_plan_device_status(jfa_plan_t plan, void* stream, int* raw);
+
+/* Human-readable text of a status code (static storage). */
+const char* jfa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JFA_H */

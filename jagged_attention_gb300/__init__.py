@@ -1,0 +1,232 @@
+"""Python binding of libjfa (jagged FlashAttention for GB300, sm_103a).
+
+Argument marshalling only: every step of the forward and backward runs in the
+CUDA kernels of ``libjfa.so`` behind the C ABI in ``include/jfa.h``.  torch is
+used for device memory and streams.  There is no fallback: if the library
+is missing or the device is not an sm_103 GPU, calls raise.
+
+    plan = Plan(kv_offsets, q_offsets=None, H=4, Lq=256, D=128)   # broadcast-Q
+    out, lse = fwd(plan, q, k, v, scale)
+    dq, dk, dv = bwd(plan, q, k, v, out, dout, lse, scale)
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+import numpy as np
+import torch
+
+PKG = Path(__file__).resolve().parent
+LIB_PATH = PKG / "libjfa.so"
+HEADER = PKG.parent / "include" / "jfa.h"
+
+JFA_OK = 0
+STATUS_NAMES = {
+    0: "JFA_OK", 1: "JFA_ERR_INVALID_ARG", 2: "JFA_ERR_UNSUPPORTED", 3: "JFA_ERR_BAD_OFFSETS",
+    4: "JFA_ERR_ALIGNMENT", 5: "JFA_ERR_WORKSPACE", 6: "JFA_ERR_CUDA", 7: "JFA_ERR_DEVICE_TIMEOUT",
+}
+BLOCK_M = BLOCK_N = 128
+
+
+class JfaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where} failed: {STATUS_NAMES.get(code, code)}")
+
+
+_lib = None
+_lib_lock = threading.Lock()
+_vp = ctypes.c_void_p
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> Path:
+    """Compile libjfa.so in-tree (nvcc, sm_103a)."""
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if not LIB_PATH.exists():
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with jagged_attention_gb300.build()")
+            L = ctypes.CDLL(str(LIB_PATH))
+            L.jfa_plan_create.argtypes = [_i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, _vp, ctypes.POINTER(_vp)]
+            L.jfa_plan_destroy.argtypes = [_vp]
+            L.jfa_plan_tiles.argtypes = [_vp, ctypes.c_int, _i32p, _i32p, _ip, _ip]
+            L.jfa_build_tiles.argtypes = [_i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, _i32p, _i32p, _ip, _ip]
+            L.jfa_fwd.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp]
+            L.jfa_bwd_workspace_bytes.argtypes = [_vp]
+            L.jfa_bwd_workspace_bytes.restype = ctypes.c_size_t
+            L.jfa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
+                                  _vp, ctypes.c_size_t, _vp]
+            L.jfa_plan_device_status.argtypes = [_vp, _vp, _ip]
+            L.jfa_status_string.argtypes = [ctypes.c_int]
+            L.jfa_status_string.restype = ctypes.c_char_p
+            for name in ("jfa_plan_create", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
+                         "jfa_fwd", "jfa_bwd", "jfa_plan_device_status"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != JFA_OK:
+        raise JfaError(rc, where)
+
+
+def _offsets(a) -> np.ndarray | None:
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _i32ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(_i32p)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def build_tiles(kv_offsets, q_offsets=None, *, H: int, Lq: int = 0, num_ctas: int, direction: int):
+    """Host-only schedule (no GPU): tiles int32 [T, 4] and cta_ptr int32 [P + 1]."""
+    kv = _offsets(kv_offsets)
+    qo = _offsets(q_offsets)
+    B = kv.size - 1
+    T, P = ctypes.c_int(), ctypes.c_int()
+    L = lib()
+    _check(L.jfa_build_tiles(_i32ptr(kv), _i32ptr(qo), B, H, Lq, num_ctas, direction, None, None,
+                             ctypes.byref(T), ctypes.byref(P)), "jfa_build_tiles")
+    tiles = np.zeros((T.value, 4), dtype=np.int32)
+    ptr = np.zeros(P.value + 1, dtype=np.int32)
+    _check(L.jfa_build_tiles(_i32ptr(kv), _i32ptr(qo), B, H, Lq, num_ctas, direction,
+                             tiles.ctypes.data_as(_i32p), ptr.ctypes.data_as(_i32p),
+                             ctypes.byref(T), ctypes.byref(P)), "jfa_build_tiles")
+    return tiles, ptr
+
+
+class Plan:
+    """A jfa_plan_t: offsets and tile schedules resident on the current device."""
+
+    def __init__(self, kv_offsets, q_offsets=None, *, H: int, D: int, Lq: int = 0,
+                 num_ctas: int = 0, stream=None):
+        self.kv_offsets = _offsets(kv_offsets)
+        self.q_offsets = _offsets(q_offsets)
+        self.B = self.kv_offsets.size - 1
+        self.H, self.D = H, D
+        self.broadcast = q_offsets is None
+        self.Lq = Lq if self.broadcast else 0
+        self.n_kv = int(self.kv_offsets[-1])
+        self.n_q = self.Lq if self.broadcast else int(self.q_offsets[-1])
+        self.n_o = self.B * self.Lq if self.broadcast else self.n_q
+        h = _vp()
+        _check(lib().jfa_plan_create(_i32ptr(self.kv_offsets), _i32ptr(self.q_offsets), self.B, H,
+                                     self.Lq, D, num_ctas, _stream(stream), ctypes.byref(h)),
+               "jfa_plan_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("plan already destroyed")
+        return self._h
+
+    def tiles(self, direction: int):
+        T, P = ctypes.c_int(), ctypes.c_int()
+        L = lib()
+        _check(L.jfa_plan_tiles(self.handle, direction, None, None, ctypes.byref(T), ctypes.byref(P)),
+               "jfa_plan_tiles")
+        tiles = np.zeros((T.value, 4), dtype=np.int32)
+        ptr = np.zeros(P.value + 1, dtype=np.int32)
+        _check(L.jfa_plan_tiles(self.handle, direction, tiles.ctypes.data_as(_i32p),
+                                ptr.ctypes.data_as(_i32p), ctypes.byref(T), ctypes.byref(P)),
+               "jfa_plan_tiles")
+        return tiles, ptr
+
+    def workspace_bytes(self) -> int:
+        return int(lib().jfa_bwd_workspace_bytes(self.handle))
+
+    def device_status(self, stream=None) -> int:
+        """Raise JfaError if a kernel recorded a timed-out wait; returns the raw word."""
+        raw = ctypes.c_int()
+        _check(lib().jfa_plan_device_status(self.handle, _stream(stream), ctypes.byref(raw)),
+               "jfa_plan_device_status")
+        return raw.value
+
+    def close(self):
+        if self._h is not None:
+            _check(lib().jfa_plan_destroy(self._h), "jfa_plan_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _dev(t: torch.Tensor, name: str, dtype) -> int:
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def fwd(plan: Plan, q, k, v, scale: float, out=None, lse=None, stream=None):
+    """O (bf16 [n_o, H, D]) and LSE (fp32 [H, n_o]) through jfa_fwd."""
+    dev = k.device if k.numel() else q.device
+    if out is None:
+        out = torch.empty((plan.n_o, plan.H, plan.D), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((plan.H, plan.n_o), dtype=torch.float32, device=dev)
+    _check(lib().jfa_fwd(plan.handle, _dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16),
+                         _dev(v, "v", torch.bfloat16), float(scale), _dev(out, "out", torch.bfloat16),
+                         _dev(lse, "lse", torch.float32), _stream(stream)), "jfa_fwd")
+    return out, lse
+
+
+def bwd(plan: Plan, q, k, v, out, dout, lse, scale: float, dq=None, dk=None, dv=None,
+        workspace=None, stream=None):
+    """dQ (fp32, shape of q), dK and dV (bf16) through jfa_bwd."""
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    ws_bytes = plan.workspace_bytes()
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=k.device)
+    _check(lib().jfa_bwd(plan.handle, _dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16),
+                         _dev(v, "v", torch.bfloat16), _dev(out, "out", torch.bfloat16),
+                         _dev(dout, "dout", torch.bfloat16), _dev(lse, "lse", torch.float32),
+                         float(scale), _dev(dq, "dq", torch.float32), _dev(dk, "dk", torch.bfloat16),
+                         _dev(dv, "dv", torch.bfloat16), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), _stream(stream)), "jfa_bwd")
+    return dq, dk, dv
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/jfa.h declares."""
+    import re
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(jfa_[a-z_0-9]+)\s*\(", text)))

@@ -1,0 +1,330 @@
+// api.cu -- the C ABI declared in include/jfa.h: argument checks, plans,
+// TMA descriptors and kernel launches.  No allocation happens in jfa_fwd /
+// jfa_bwd; plans own their (small) device copies of offsets and schedules.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/jfa.h"
+#include "kernels.h"
+#include "plan.h"
+
+using jfa::Schedule;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// TMA descriptor of a packed bf16 tensor viewed as 2-D [rows, H*D]: boxes of
+// 128 rows x 64 columns (128 bytes) with the 128-byte swizzle the MMA
+// descriptors expect.  Rows past the end read as zeros.  An empty tensor gets
+// a zeroed descriptor that no tile ever uses.
+int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+  std::memset(m, 0, sizeof(*m));
+  if (rows == 0) return JFA_OK;
+  auto enc = tensor_map_encoder();
+  if (!enc) return JFA_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? JFA_OK : JFA_ERR_CUDA;
+}
+
+jfa::Problem problem_of(const jfa_plan* p) {
+  jfa::Problem pb;
+  pb.kv_off = p->d_kv_off;
+  pb.q_off = p->d_q_off;
+  pb.B = p->B;
+  pb.H = p->H;
+  pb.Lq = p->Lq;
+  pb.D = p->D;
+  pb.n_q = p->n_q;
+  pb.n_o = p->n_o;
+  pb.n_kv = p->n_kv;
+  return pb;
+}
+
+// Lengths from host offsets; q_off == nullptr means broadcast with Lq rows.
+int lengths_of(const int32_t* kv_off, const int32_t* q_off, int B, int Lq,
+               std::vector<int64_t>& qlen, std::vector<int64_t>& kvlen, int64_t* n_kv,
+               int64_t* n_q) {
+  if (!jfa::validate_offsets(kv_off, B, n_kv)) return JFA_ERR_BAD_OFFSETS;
+  if (q_off) {
+    if (!jfa::validate_offsets(q_off, B, n_q)) return JFA_ERR_BAD_OFFSETS;
+  } else {
+    if (Lq < 0) return JFA_ERR_INVALID_ARG;
+    *n_q = Lq;
+  }
+  qlen.resize(B);
+  kvlen.resize(B);
+  for (int b = 0; b < B; ++b) {
+    kvlen[b] = kv_off[b + 1] - kv_off[b];
+    qlen[b] = q_off ? (q_off[b + 1] - q_off[b]) : Lq;
+  }
+  return JFA_OK;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* jfa_status_string(int s) {
+  switch (s) {
+    case JFA_OK: return "ok";
+    case JFA_ERR_INVALID_ARG: return "invalid argument";
+    case JFA_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case JFA_ERR_BAD_OFFSETS: return "bad offsets";
+    case JFA_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case JFA_ERR_WORKSPACE: return "workspace missing or too small";
+    case JFA_ERR_CUDA: return "CUDA runtime error";
+    case JFA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                    int Lq, int num_ctas, int dir, int32_t* tiles_out, int32_t* cta_ptr_out, int* T,
+                    int* P) {
+  if (!kv_offsets_host || B < 1 || H < 1 || num_ctas < 1 || (dir != 0 && dir != 1) || !T || !P)
+    return JFA_ERR_INVALID_ARG;
+  std::vector<int64_t> qlen, kvlen;
+  int64_t n_kv = 0, n_q = 0;
+  int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
+  if (rc != JFA_OK) return rc;
+  const Schedule s = dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas)
+                              : jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas);
+  *T = s.T;
+  *P = s.P;
+  if (tiles_out) std::memcpy(tiles_out, s.tiles.data(), s.tiles.size() * sizeof(int32_t));
+  if (cta_ptr_out) std::memcpy(cta_ptr_out, s.cta_ptr.data(), s.cta_ptr.size() * sizeof(int32_t));
+  return JFA_OK;
+}
+
+int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                    int Lq, int D, int num_ctas, void* stream, jfa_plan_t* out) {
+  if (!out || !kv_offsets_host || B < 1 || H < 1 || num_ctas < 0) return JFA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+  std::vector<int64_t> qlen, kvlen;
+  int64_t n_kv = 0, n_q = 0;
+  int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
+  if (rc != JFA_OK) return rc;
+  const int64_t n_o = q_offsets_host ? n_q : int64_t(B) * Lq;
+  if (n_o >= (int64_t(1) << 31) || int64_t(H) * D * 2 >= (int64_t(1) << 31))
+    return JFA_ERR_UNSUPPORTED;
+
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  if (major != 10 || minor != 3) return JFA_ERR_UNSUPPORTED;  // built for sm_103a only
+
+  auto* p = new jfa_plan();
+  p->B = B;
+  p->H = H;
+  p->Lq = q_offsets_host ? 0 : Lq;
+  p->D = D;
+  p->broadcast = q_offsets_host == nullptr;
+  p->device = dev;
+  p->num_ctas = num_ctas > 0 ? num_ctas : sms;
+  p->n_q = n_q;
+  p->n_o = n_o;
+  p->n_kv = n_kv;
+  p->fwd = jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas);
+  p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas);
+  for (int b = 0; b < B; ++b) {
+    if (qlen[b] == 0 && kvlen[b] > 0) {
+      const int64_t s = kv_offsets_host[b], e = kv_offsets_host[b + 1];
+      if (!p->kv_rows_without_queries.empty() && p->kv_rows_without_queries.back().second == s)
+        p->kv_rows_without_queries.back().second = e;
+      else
+        p->kv_rows_without_queries.emplace_back(s, e);
+    }
+  }
+
+  // one device block: offsets, schedules, status word (16-byte aligned pieces)
+  const size_t o_kv = 0;
+  const size_t o_q = align_up(o_kv + (B + 1) * 4, 16);
+  const size_t o_ft = align_up(o_q + (q_offsets_host ? (B + 1) * 4 : 0), 16);
+  const size_t o_fp = align_up(o_ft + p->fwd.tiles.size() * 4, 16);
+  const size_t o_bt = align_up(o_fp + p->fwd.cta_ptr.size() * 4, 16);
+  const size_t o_bp = align_up(o_bt + p->bwd.tiles.size() * 4, 16);
+  const size_t o_st = align_up(o_bp + p->bwd.cta_ptr.size() * 4, 16);
+  const size_t bytes = align_up(o_st + 16, 256);
+  std::vector<uint8_t> host(bytes, 0);
+  std::memcpy(&host[o_kv], kv_offsets_host, (B + 1) * 4);
+  if (q_offsets_host) std::memcpy(&host[o_q], q_offsets_host, (B + 1) * 4);
+  if (!p->fwd.tiles.empty()) std::memcpy(&host[o_ft], p->fwd.tiles.data(), p->fwd.tiles.size() * 4);
+  std::memcpy(&host[o_fp], p->fwd.cta_ptr.data(), p->fwd.cta_ptr.size() * 4);
+  if (!p->bwd.tiles.empty()) std::memcpy(&host[o_bt], p->bwd.tiles.data(), p->bwd.tiles.size() * 4);
+  std::memcpy(&host[o_bp], p->bwd.cta_ptr.data(), p->bwd.cta_ptr.size() * 4);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMalloc(&p->dev_block, bytes) != cudaSuccess) {
+    delete p;
+    return JFA_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(p->dev_block, host.data(), bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaFree(p->dev_block);
+    delete p;
+    return JFA_ERR_CUDA;
+  }
+  auto* base = static_cast<uint8_t*>(p->dev_block);
+  p->d_kv_off = reinterpret_cast<int32_t*>(base + o_kv);
+  p->d_q_off = q_offsets_host ? reinterpret_cast<int32_t*>(base + o_q) : nullptr;
+  p->d_fwd_tiles = reinterpret_cast<int32_t*>(base + o_ft);
+  p->d_fwd_ptr = reinterpret_cast<int32_t*>(base + o_fp);
+  p->d_bwd_tiles = reinterpret_cast<int32_t*>(base + o_bt);
+  p->d_bwd_ptr = reinterpret_cast<int32_t*>(base + o_bp);
+  p->d_status = reinterpret_cast<int*>(base + o_st);
+  *out = p;
+  return JFA_OK;
+}
+
+int jfa_plan_destroy(jfa_plan_t plan) {
+  if (!plan) return JFA_ERR_INVALID_ARG;
+  int rc = JFA_OK;
+  if (plan->dev_block && cudaFree(plan->dev_block) != cudaSuccess) rc = JFA_ERR_CUDA;
+  delete plan;
+  return rc;
+}
+
+int jfa_plan_tiles(jfa_plan_t plan, int dir, int32_t* tiles_host, int32_t* cta_ptr_host, int* T,
+                   int* P) {
+  if (!plan || (dir != 0 && dir != 1) || !T || !P) return JFA_ERR_INVALID_ARG;
+  const Schedule& s = dir == 0 ? plan->fwd : plan->bwd;
+  *T = s.T;
+  *P = s.P;
+  if (tiles_host) std::memcpy(tiles_host, s.tiles.data(), s.tiles.size() * sizeof(int32_t));
+  if (cta_ptr_host) std::memcpy(cta_ptr_host, s.cta_ptr.data(), s.cta_ptr.size() * sizeof(int32_t));
+  return JFA_OK;
+}
+
+int jfa_plan_device_status(jfa_plan_t plan, void* stream, int* raw) {
+  if (!plan) return JFA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  if (raw) *raw = word;
+  if (word != 0) {
+    if (cudaMemsetAsync(plan->d_status, 0, sizeof(int), s) != cudaSuccess) return JFA_ERR_CUDA;
+    return JFA_ERR_DEVICE_TIMEOUT;
+  }
+  return JFA_OK;
+}
+
+int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float scale, void* out,
+            float* lse, void* stream) {
+  if (!plan || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if ((plan->n_q > 0 && !q) || (plan->n_kv > 0 && (!k || !v)) || (plan->n_o > 0 && (!out || !lse)))
+    return JFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return JFA_ERR_ALIGNMENT;
+  if (plan->fwd.P == 0) return JFA_OK;
+  const int64_t cols = int64_t(plan->H) * plan->D;
+  CUtensorMap qm, km, vm;
+  if (make_map(&qm, q, plan->n_q, cols) || make_map(&km, k, plan->n_kv, cols) ||
+      make_map(&vm, v, plan->n_kv, cols))
+    return JFA_ERR_CUDA;
+  jfa::FwdArgs a;
+  a.pb = problem_of(plan);
+  a.tiles = plan->d_fwd_tiles;
+  a.cta_ptr = plan->d_fwd_ptr;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.status = plan->d_status;
+  cudaError_t e = jfa::launch_fwd(a, qm, km, vm, plan->fwd.P, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+size_t jfa_bwd_workspace_bytes(jfa_plan_t plan) {
+  if (!plan) return 0;
+  return align_up(static_cast<size_t>(plan->n_o) * plan->H * sizeof(float), 256);
+}
+
+int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const void* out,
+            const void* dout, const float* lse, float scale, float* dq, void* dk, void* dv,
+            void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if ((plan->n_q > 0 && (!q || !dq)) || (plan->n_kv > 0 && (!k || !v || !dk || !dv)) ||
+      (plan->n_o > 0 && (!out || !dout || !lse)))
+    return JFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return JFA_ERR_ALIGNMENT;
+  const size_t need = jfa_bwd_workspace_bytes(plan);
+  if (plan->n_o > 0 && (!workspace || workspace_bytes < need)) return JFA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t cols = int64_t(plan->H) * plan->D;
+  float* delta = static_cast<float*>(workspace);
+
+  // dQ is reduce-added by the key/value tiles: start from zero
+  if (plan->n_q > 0 &&
+      cudaMemsetAsync(dq, 0, static_cast<size_t>(plan->n_q) * cols * sizeof(float), s) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  // keys of sequences without queries get no backward tile: their gradients are zero
+  for (const auto& run : plan->kv_rows_without_queries) {
+    const size_t off = static_cast<size_t>(run.first) * cols * 2;
+    const size_t len = static_cast<size_t>(run.second - run.first) * cols * 2;
+    if (cudaMemsetAsync(static_cast<uint8_t*>(dk) + off, 0, len, s) != cudaSuccess ||
+        cudaMemsetAsync(static_cast<uint8_t*>(dv) + off, 0, len, s) != cudaSuccess)
+      return JFA_ERR_CUDA;
+  }
+  if (plan->bwd.P == 0) return JFA_OK;
+  cudaError_t e = jfa::launch_delta(static_cast<const uint16_t*>(out),
+                                    static_cast<const uint16_t*>(dout), delta, plan->n_o, plan->H,
+                                    plan->D, s);
+  if (e != cudaSuccess) return JFA_ERR_CUDA;
+  CUtensorMap qm, km, vm, dom;
+  if (make_map(&qm, q, plan->n_q, cols) || make_map(&km, k, plan->n_kv, cols) ||
+      make_map(&vm, v, plan->n_kv, cols) || make_map(&dom, dout, plan->n_o, cols))
+    return JFA_ERR_CUDA;
+  jfa::BwdArgs a;
+  a.pb = problem_of(plan);
+  a.tiles = plan->d_bwd_tiles;
+  a.cta_ptr = plan->d_bwd_ptr;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.lse = lse;
+  a.delta = delta;
+  a.dq = dq;
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.status = plan->d_status;
+  e = jfa::launch_bwd(a, qm, km, vm, dom, plan->bwd.P, s);
+  if (e == cudaErrorNotSupported) return JFA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,428 @@
+// fwd.cu -- jagged FlashAttention forward for GB300 (sm_103a).
+//
+// One persistent CTA per SM walks its slice of the host-built schedule
+// (tiles (b, h, query block m), zigzag-dealt by key/value cost).  For each
+// tile it streams the sequence's key/value blocks through a TMA-fed shared
+// memory ring and runs FlashAttention's online softmax:
+//
+//   S_j = Q K_j^T                  tcgen05.mma, fp32 accumulator in TMEM
+//   m, l   running row max / sum   fp32 in registers, exp2 with scale*log2(e) folded in
+//   P_j = exp2(S_j*c - m)          bf16, written back into TMEM
+//   O  += P_j V_j                  tcgen05.mma with A = P_j from TMEM
+//   O  /= l, LSE = m ln2 + ln l    epilogue
+//
+// The structure follows the roles the jagged FlashAttention pages describe
+// (alphasignal page, "Specialized warps keep tensor cores busy": a load warp,
+// an MMA warp, softmax/correction warps, output stores; a multi-stage K/V
+// pipeline; persistent CTAs), re-derived for sm_103a:
+//   warp 4      TMA producer (Q once per tile, K and V per block)
+//   warp 5      tcgen05.mma issuer; owns the TMEM allocation
+//   warps 0-3   softmax + correction + epilogue, one thread per query row
+// TMEM (512 columns): two 128-column score buffers (so QK^T of block j+1
+// overlaps the softmax of block j), the D-column O accumulator and two
+// 64-column bf16 P buffers.  O is rescaled only when a row's max grows by
+// more than 2^8 (the stale max keeps every P <= 256, exact after the final
+// division by l).  The last, partial key block is the only one that masks
+// (the pages' "loop peeling": the bulk pass is branch-free).
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace jfa {
+namespace {
+
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kChunks = D / 64;             // 128-byte column chunks per row
+  static constexpr int kChunkBytes = 128 * 128;      // one [128 rows x 64 bf16] chunk
+  static constexpr int kTileBytes = 128 * D * 2;     // one 128-row tile of Q, K or V
+  static constexpr int kStages = (D == 128) ? 3 : 4; // K and V ring depth (keeps 1 CTA/SM)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+  static constexpr uint32_t kColS = 0;               // 2 x 128 fp32 columns
+  static constexpr uint32_t kColO = 256;             // D fp32 columns
+  static constexpr uint32_t kColP = 256 + D;         // 2 x 64 columns of bf16 pairs
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 192;
+  static constexpr int kProducerWarp = 4;
+  static constexpr int kMmaWarp = 5;
+};
+
+struct FwdBars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t o_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct Tile {
+  int b, h, blk, cost;
+};
+__device__ __forceinline__ Tile load_tile(const int32_t* tiles, int i) {
+  const int4 t = __ldg(reinterpret_cast<const int4*>(tiles) + i);
+  return {t.x, t.y, t.z, t.w};
+}
+
+// Wait with every lane of the warp, and agree on the outcome so that the
+// warp stays converged for the .sync.aligned tcgen05 instructions after it.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
+}
+
+// Bounded wait used only while draining at exit: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA producer (one thread)
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const CUtensorMap* k_map,
+                             const CUtensorMap* v_map, uint32_t sbase, FwdBars& bars,
+                             const Abort& ab, int t_begin, int t_end) {
+  using C = FwdCfg<D>;
+  tma_prefetch_desc(q_map);
+  tma_prefetch_desc(k_map);
+  tma_prefetch_desc(v_map);
+  const uint32_t sQ = sbase + C::kOffQ;
+  uint32_t nq = 0, nk = 0, nv = 0;  // loads issued
+  bool ok = true;
+  for (int i = t_begin; i < t_end && ok; ++i) {
+    const Tile t = load_tile(a.tiles, i);
+    if (t.cost == 0) continue;
+    const int kv0 = a.pb.kv_off[t.b];
+    const int qrow = (a.pb.q_off ? a.pb.q_off[t.b] : 0) + t.blk * 128;
+    const int x0 = t.h * D;
+    ok = mbar_wait(smem_u32(&bars.q_empty), (nq & 1) ^ 1, ab);
+    if (!ok) break;
+    mbar_arrive_expect_tx(smem_u32(&bars.q_full), C::kTileBytes);
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c)
+      tma_load_2d(sQ + c * C::kChunkBytes, q_map, smem_u32(&bars.q_full), x0 + c * 64, qrow);
+    ++nq;
+    for (int j = 0; j < t.cost && ok; ++j) {
+      const uint32_t st = nk % C::kStages, ph = (nk / C::kStages) & 1;
+      const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
+      const uint32_t sV = sbase + C::kOffV + st * C::kTileBytes;
+      ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, ab);
+      if (!ok) break;
+      mbar_arrive_expect_tx(smem_u32(&bars.k_full[st]), C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_2d(sK + c * C::kChunkBytes, k_map, smem_u32(&bars.k_full[st]), x0 + c * 64,
+                    kv0 + j * 128);
+      ++nk;
+      ok = mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, ab);
+      if (!ok) break;
+      mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_2d(sV + c * C::kChunkBytes, v_map, smem_u32(&bars.v_full[st]), x0 + c * 64,
+                    kv0 + j * 128);
+      ++nv;
+    }
+  }
+  // Let every copy this thread issued land before the CTA can exit: the last
+  // phase issued on each full barrier completes when its bytes arrive, and
+  // nothing else completes phases of the full barriers.
+  if (nq > 0) drain_wait(smem_u32(&bars.q_full), (nq - 1) & 1);
+  for (uint32_t st = 0; st < C::kStages; ++st) {
+    if (st < nk) {
+      const uint32_t last = nk - 1 - ((nk - 1 - st) % C::kStages);  // last K load into stage st
+      drain_wait(smem_u32(&bars.k_full[st]), (last / C::kStages) & 1);
+    }
+    if (st < nv) {
+      const uint32_t last = nv - 1 - ((nv - 1 - st) % C::kStages);
+      drain_wait(smem_u32(&bars.v_full[st]), (last / C::kStages) & 1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread)
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars& bars,
+                        const Abort& ab, int t_begin, int t_end) {
+  using C = FwdCfg<D>;
+  constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+  const uint32_t sQ = sbase + C::kOffQ;
+  uint32_t g = 0, tq = 0;
+
+  // O += P_gp V_gp; `first` marks the first block of a tile (overwrite O).
+  auto issue_pv = [&](uint32_t gp, bool first) -> bool {
+    const uint32_t pb = gp & 1, st = gp % C::kStages;
+    if (first && !mbar_wait(smem_u32(&bars.o_empty), (tq & 1) ^ 1, ab)) return false;
+    if (!mbar_wait(smem_u32(&bars.p_full[pb]), (gp >> 1) & 1, ab)) return false;
+    if (!mbar_wait(smem_u32(&bars.v_full[st]), (gp / C::kStages) & 1, ab)) return false;
+    tc_fence_after();
+    const uint32_t sV = sbase + C::kOffV + st * C::kTileBytes;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t vdesc = smem_desc_sw128(sV + kk * 2048, C::kChunkBytes, 1024);
+      mma_bf16_ts(tmem + C::kColO, tmem + C::kColP + pb * 64 + kk * 8, vdesc, idesc_pv,
+                  (first && kk == 0) ? 0u : 1u);
+    }
+    mma_commit(smem_u32(&bars.v_empty[st]));
+    mma_commit(smem_u32(&bars.pv_done[pb]));
+    return true;
+  };
+
+  bool ok = true;
+  for (int i = t_begin; i < t_end && ok; ++i) {
+    const Tile t = load_tile(a.tiles, i);
+    if (t.cost == 0) continue;
+    ok = mbar_wait(smem_u32(&bars.q_full), tq & 1, ab);
+    for (int j = 0; j < t.cost && ok; ++j) {
+      const uint32_t gj = g + j, st = gj % C::kStages, sb = gj & 1;
+      ok = mbar_wait(smem_u32(&bars.k_full[st]), (gj / C::kStages) & 1, ab) &&
+           mbar_wait(smem_u32(&bars.s_empty[sb]), ((gj >> 1) & 1) ^ 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+        mma_bf16_ss(tmem + C::kColS + sb * 128, smem_desc_sw128(sQ + koff, 16, 1024),
+                    smem_desc_sw128(sK + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&bars.s_full[sb]));
+      mma_commit(smem_u32(&bars.k_empty[st]));
+      if (j == t.cost - 1) mma_commit(smem_u32(&bars.q_empty));
+      if (j >= 1) ok = issue_pv(gj - 1, j == 1);
+    }
+    if (ok) ok = issue_pv(g + t.cost - 1, t.cost == 1);
+    g += t.cost;
+    ++tq;
+  }
+  // every MMA issued above has completed once this commit arrives
+  mma_commit(smem_u32(&bars.drain));
+  drain_wait(smem_u32(&bars.drain), 0);
+}
+
+// ---------------------------------------------------------------------------
+// softmax / correction / epilogue (warps 0-3, thread = query row = TMEM lane)
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, const Abort& ab,
+                            int t_begin, int t_end) {
+  using C = FwdCfg<D>;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = tid;  // row of the tile, TMEM lane
+  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const float sl2 = a.scale_log2;
+  const int H = a.pb.H;
+  uint32_t g = 0;
+
+  for (int i = t_begin; i < t_end; ++i) {
+    const Tile t = load_tile(a.tiles, i);
+    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + 1] - a.pb.q_off[t.b]) : a.pb.Lq;
+    const int64_t o_first = (a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq) + t.blk * 128;
+    const bool row_ok = int64_t(t.blk) * 128 + r < qlen;
+    const int64_t orow = o_first + r;
+    uint16_t* orow_ptr = a.out + (orow * H + t.h) * D;
+    if (t.cost == 0) {  // no keys: O = 0, LSE = -inf
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(orow_ptr);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        a.lse[int64_t(t.h) * a.pb.n_o + orow] = -INFINITY;
+      }
+      continue;
+    }
+    const int last_valid = (a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b]) - (t.cost - 1) * 128;
+    float m_run = -INFINITY, l_run = 0.0f;
+    for (int j = 0; j < t.cost; ++j) {
+      const uint32_t gj = g + j, sb = gj & 1;
+      if (!warp_wait(smem_u32(&bars.s_full[sb]), (gj >> 1) & 1, ab)) return;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_x32(tl + C::kColS + sb * 128 + c * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.s_empty[sb]));
+      if (j == t.cost - 1 && last_valid < 128) {  // peeled tail: mask keys past the sequence
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (e >= last_valid) s[e] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, s[e]);
+      const float m_cand = mx * sl2;
+      const bool resc = m_cand > m_run + kRescaleThreshold;
+      const float m_new = resc ? m_cand : m_run;
+      const float alpha = resc ? fast_exp2(m_run - m_new) : 1.0f;
+      uint32_t p[64];
+      float rowsum = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        const float p0 = fast_exp2(fmaf(s[2 * e], sl2, -m_new));
+        const float p1 = fast_exp2(fmaf(s[2 * e + 1], sl2, -m_new));
+        p[e] = pack_bf16x2(p0, p1);
+        // normalise by the sum of the rounded weights the PV product uses, so
+        // O stays an exact convex combination of V rows under those weights
+        rowsum += __uint_as_float(p[e] << 16) + __uint_as_float(p[e] & 0xffff0000u);
+      }
+      l_run = l_run * alpha + rowsum;
+      // the P buffer is free once PV of block gj-2 has completed
+      if (!warp_wait(smem_u32(&bars.pv_done[sb]), ((gj >> 1) & 1) ^ 1, ab)) return;
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        const uint32_t gp = gj - 1;  // O must hold PV of block gj-1 before rescaling
+        if (!warp_wait(smem_u32(&bars.pv_done[gp & 1]), (gp >> 1) & 1, ab)) return;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_x32(tl + C::kColO + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st_x32(tl + C::kColO + c * 32, v);
+        }
+      }
+      {
+        uint32_t lo[32], hi[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          lo[e] = p[e];
+          hi[e] = p[32 + e];
+        }
+        tmem_st_x32(tl + C::kColP + sb * 64, lo);
+        tmem_st_x32(tl + C::kColP + sb * 64 + 32, hi);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.p_full[sb]));
+      m_run = m_new;
+    }
+    // epilogue: wait for the last PV, normalise, store O and LSE
+    const uint32_t gl = g + t.cost - 1;
+    if (!warp_wait(smem_u32(&bars.pv_done[gl & 1]), (gl >> 1) & 1, ab)) return;
+    tc_fence_after();
+    const float inv_l = 1.0f / l_run;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld_x32(tl + C::kColO + c * 32, v);
+      if (row_ok) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(orow_ptr + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&bars.o_empty));
+    if (row_ok) a.lse[int64_t(t.h) * a.pb.n_o + orow] = (m_run + __log2f(l_run)) * kLn2;
+    g += t.cost;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+    jfa_fwd_kernel(const __grid_constant__ CUtensorMap q_map,
+                   const __grid_constant__ CUtensorMap k_map,
+                   const __grid_constant__ CUtensorMap v_map, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  FwdBars& bars = *reinterpret_cast<FwdBars*>(smem + C::kOffBar);
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t_begin = a.cta_ptr[blockIdx.x], t_end = a.cta_ptr[blockIdx.x + 1];
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars.q_full), 1);
+    mbar_init(smem_u32(&bars.q_empty), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&bars.k_full[s]), 1);
+      mbar_init(smem_u32(&bars.k_empty[s]), 1);
+      mbar_init(smem_u32(&bars.v_full[s]), 1);
+      mbar_init(smem_u32(&bars.v_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars.s_full[s]), 1);
+      mbar_init(smem_u32(&bars.s_empty[s]), 128);
+      mbar_init(smem_u32(&bars.p_full[s]), 128);
+      mbar_init(smem_u32(&bars.pv_done[s]), 1);
+    }
+    mbar_init(smem_u32(&bars.o_empty), 128);
+    mbar_init(smem_u32(&bars.drain), 1);
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(smem_u32(&bars.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const Abort ab{&bars.abort_flag, a.status};
+
+  if (warp == C::kProducerWarp) {
+    if (lane == 0) fwd_producer<D>(a, &q_map, &k_map, &v_map, sbase, bars, ab, t_begin, t_end);
+    __syncwarp();
+  } else if (warp == C::kMmaWarp) {
+    if (lane == 0) fwd_mma<D>(a, sbase, tmem, bars, ab, t_begin, t_end);
+    __syncwarp();
+  } else {
+    fwd_softmax<D>(a, tmem, bars, ab, t_begin, t_end);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
+                         const CUtensorMap& v, int grid, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  static_assert(C::kSmemBytes <= 232448, "shared memory budget");
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  jfa_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                       const CUtensorMap& v_map, int grid, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  if (a.pb.D == 128) return launch_fwd_d<128>(a, q_map, k_map, v_map, grid, stream);
+  return launch_fwd_d<64>(a, q_map, k_map, v_map, grid, stream);
+}
+
+}  // namespace jfa

@@ -1,0 +1,56 @@
+// kernels.h -- parameter blocks and launchers of the device kernels (internal).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace jfa {
+
+// Problem description shared by every kernel.  Offsets are device int32
+// [B+1]; q_off == nullptr selects broadcast mode (Q has Lq rows shared by all
+// sequences, O / dO / LSE have B*Lq rows, b-major).
+struct Problem {
+  const int32_t* kv_off;
+  const int32_t* q_off;
+  int B, H, Lq, D;
+  int64_t n_q, n_o, n_kv;
+};
+
+struct FwdArgs {
+  Problem pb;
+  const int32_t* tiles;    // [T][4] {b, h, m, cost}
+  const int32_t* cta_ptr;  // [P+1]
+  float scale_log2;        // scale * log2(e)
+  uint16_t* out;           // bf16 [n_o, H, D]
+  float* lse;              // [H, n_o]
+  int* status;
+};
+
+struct BwdArgs {
+  Problem pb;
+  const int32_t* tiles;    // [T][4] {b, h, n, qblocks}
+  const int32_t* cta_ptr;
+  float scale;             // softmax scale
+  float scale_log2;        // scale * log2(e)
+  const float* lse;        // [H, n_o]
+  const float* delta;      // [H, n_o]
+  float* dq;               // fp32 [n_q, H, D]
+  uint16_t* dk;            // bf16 [n_kv, H, D]
+  uint16_t* dv;
+  int* status;
+};
+
+// Forward: one persistent launch over the schedule (grid = P CTAs).
+cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                       const CUtensorMap& v_map, int grid, cudaStream_t stream);
+
+// Backward pre-pass: delta[h, i] = sum_d dO[i,h,d] * O[i,h,d].
+cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta, int64_t n_o,
+                         int H, int D, cudaStream_t stream);
+
+// Backward main pass (grid = P CTAs).
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                       const CUtensorMap& v_map, const CUtensorMap& do_map, int grid,
+                       cudaStream_t stream);
+
+}  // namespace jfa

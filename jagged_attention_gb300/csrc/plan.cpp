@@ -1,0 +1,104 @@
+// plan.cpp -- host-side tile schedules for the persistent kernels.
+//
+// Forward: the jagged FlashAttention pages balance forward work on the host:
+// tiles are sorted by key/value workload and dealt to the SMs back and forth
+// (alphasignal page, "Five changes unlocked the gains", item 1; yuxiaoba
+// note, "Why both static and dynamic balancing help").  Backward: the valid
+// (batch, head, key/value-block) tiles are precomputed and dealt round-robin
+// (same note; asivanadi0 blog, "Structural changes and layered opts",
+// item 1).  The exact order (enumeration b, h, block; stable sort by cost
+// descending; CTA k on even rounds, P-1-k on odd rounds) is this library's
+// reading of those passages.
+#include "plan.h"
+
+#include <algorithm>
+#include <numeric>
+
+namespace jfa {
+
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool validate_offsets(const int32_t* off, int B, int64_t* total) {
+  if (off == nullptr || B < 1) return false;
+  if (off[0] != 0) return false;
+  for (int b = 0; b < B; ++b)
+    if (off[b + 1] < off[b]) return false;
+  // int32 offsets already bound the total below 2^31
+  *total = off[B];
+  return true;
+}
+
+Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
+                            int H, int num_ctas) {
+  const int B = static_cast<int>(q_len.size());
+  std::vector<int32_t> flat;  // enumeration order
+  for (int b = 0; b < B; ++b) {
+    const int32_t cost = static_cast<int32_t>(cdiv(kv_len[b], kBN));
+    const int64_t mblocks = cdiv(q_len[b], kBM);
+    for (int h = 0; h < H; ++h)
+      for (int64_t m = 0; m < mblocks; ++m) {
+        flat.push_back(b);
+        flat.push_back(h);
+        flat.push_back(static_cast<int32_t>(m));
+        flat.push_back(cost);
+      }
+  }
+  Schedule s;
+  s.T = static_cast<int>(flat.size() / 4);
+  s.P = std::min(num_ctas, s.T);
+  s.cta_ptr.assign(s.P + 1, 0);
+  if (s.T == 0) return s;
+  std::vector<int> order(s.T);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return flat[4 * a + 3] > flat[4 * b + 3]; });
+  // deal: sorted tile i -> round i / P, position i % P, zigzag across rounds
+  std::vector<int> cta_of(s.T);
+  for (int i = 0; i < s.T; ++i) {
+    const int r = i / s.P, k = i % s.P;
+    cta_of[i] = (r % 2 == 0) ? k : s.P - 1 - k;
+    ++s.cta_ptr[cta_of[i] + 1];
+  }
+  for (int c = 0; c < s.P; ++c) s.cta_ptr[c + 1] += s.cta_ptr[c];
+  s.tiles.resize(4 * static_cast<size_t>(s.T));
+  std::vector<int32_t> fill(s.cta_ptr.begin(), s.cta_ptr.end() - 1);
+  for (int i = 0; i < s.T; ++i) {  // i increases with the round, so each CTA's list is in round order
+    const int dst = fill[cta_of[i]]++;
+    std::copy_n(&flat[4 * static_cast<size_t>(order[i])], 4, &s.tiles[4 * static_cast<size_t>(dst)]);
+  }
+  return s;
+}
+
+Schedule build_bwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
+                            int H, int num_ctas) {
+  const int B = static_cast<int>(q_len.size());
+  std::vector<int32_t> flat;
+  for (int b = 0; b < B; ++b) {
+    if (q_len[b] == 0) continue;
+    const int32_t qblocks = static_cast<int32_t>(cdiv(q_len[b], kBM));
+    const int64_t nblocks = cdiv(kv_len[b], kBN);
+    for (int h = 0; h < H; ++h)
+      for (int64_t n = 0; n < nblocks; ++n) {
+        flat.push_back(b);
+        flat.push_back(h);
+        flat.push_back(static_cast<int32_t>(n));
+        flat.push_back(qblocks);
+      }
+  }
+  Schedule s;
+  s.T = static_cast<int>(flat.size() / 4);
+  s.P = std::min(num_ctas, s.T);
+  s.cta_ptr.assign(s.P + 1, 0);
+  if (s.T == 0) return s;
+  for (int i = 0; i < s.T; ++i) ++s.cta_ptr[i % s.P + 1];
+  for (int c = 0; c < s.P; ++c) s.cta_ptr[c + 1] += s.cta_ptr[c];
+  s.tiles.resize(4 * static_cast<size_t>(s.T));
+  std::vector<int32_t> fill(s.cta_ptr.begin(), s.cta_ptr.end() - 1);
+  for (int i = 0; i < s.T; ++i) {
+    const int dst = fill[i % s.P]++;
+    std::copy_n(&flat[4 * static_cast<size_t>(i)], 4, &s.tiles[4 * static_cast<size_t>(dst)]);
+  }
+  return s;
+}
+
+}  // namespace jfa

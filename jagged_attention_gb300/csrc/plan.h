@@ -1,0 +1,58 @@
+// plan.h -- host-side tile schedules and the plan object behind jfa_plan_t.
+#pragma once
+#include <cstdint>
+#include <utility>
+#include <vector>
+
+namespace jfa {
+
+constexpr int kBM = 128;  // query rows per forward tile / per backward query block
+constexpr int kBN = 128;  // key rows per key/value block / per backward tile
+
+// A schedule: T tiles of four int32 {b, h, block, cost}, grouped by CTA, and
+// the CSR row pointer over the P CTAs that receive work.
+struct Schedule {
+  std::vector<int32_t> tiles;    // 4 * T
+  std::vector<int32_t> cta_ptr;  // P + 1
+  int T = 0;
+  int P = 0;
+};
+
+// Check offsets: off[0] == 0, non-decreasing, total < 2^31.  Returns the
+// total through *total.  false on any violation.
+bool validate_offsets(const int32_t* off, int B, int64_t* total);
+
+// Forward schedule: tiles (b, h, m) for m < ceil(Lq_b / BM) with cost
+// ceil(Lk_b / BN), stable-sorted by cost descending, dealt zigzag to
+// P = min(num_ctas, T) CTAs.
+Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
+                            int H, int num_ctas);
+// Backward schedule: tiles (b, h, n) for n < ceil(Lk_b / BN) where Lq_b > 0,
+// cost ceil(Lq_b / BM), dealt round-robin.
+Schedule build_bwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
+                            int H, int num_ctas);
+
+}  // namespace jfa
+
+struct jfa_plan {
+  int B = 0, H = 0, Lq = 0, D = 0;
+  bool broadcast = false;
+  int device = 0;
+  int num_ctas = 0;
+  int64_t n_q = 0;   // rows of Q
+  int64_t n_o = 0;   // rows of O / dO / LSE
+  int64_t n_kv = 0;  // rows of K / V
+  jfa::Schedule fwd, bwd;
+  // key/value row ranges [begin, end) of sequences that have keys but no
+  // queries: no backward tile covers them, so their dK / dV are cleared
+  std::vector<std::pair<int64_t, int64_t>> kv_rows_without_queries;
+  // device copies (one allocation)
+  void* dev_block = nullptr;
+  int32_t* d_kv_off = nullptr;
+  int32_t* d_q_off = nullptr;  // null in broadcast mode
+  int32_t* d_fwd_tiles = nullptr;
+  int32_t* d_fwd_ptr = nullptr;
+  int32_t* d_bwd_tiles = nullptr;
+  int32_t* d_bwd_ptr = nullptr;
+  int* d_status = nullptr;
+};

@@ -1,0 +1,88 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI and
+compare with the fp64 oracle on the same seeded inputs.
+
+Tolerances (bf16 inputs, fp32 accumulation): O max-abs <= 1e-2, LSE max-abs
+<= 1e-3, relative L2 <= 1e-2 for dQ, dK and dV.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import jagged_attention_gb300 as jfa
+import oracle
+import workloads
+
+TOL_O = 1e-2
+TOL_LSE = 1e-3
+TOL_GRAD = 1e-2
+
+
+def to_cuda(p: workloads.Problem) -> workloads.Problem:
+    return workloads.Problem(p.B, p.H, p.D, p.mode, p.Lq, p.kv_offsets, p.q_offsets,
+                             p.q.cuda(), p.k.cuda(), p.v.cuda(), p.dout.cuda(), p.scale)
+
+
+def make_plan(p: workloads.Problem, num_ctas: int = 0) -> jfa.Plan:
+    return jfa.Plan(p.kv_offsets, p.q_offsets, H=p.H, D=p.D, Lq=p.Lq, num_ctas=num_ctas)
+
+
+def gpu_fwd(p: workloads.Problem, plan: jfa.Plan | None = None):
+    """O, LSE from the CUDA path; outputs are NaN-prefilled so unwritten rows show up."""
+    plan = plan or make_plan(p)
+    out = torch.full((p.n_o_rows, p.H, p.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((p.H, p.n_o_rows), float("nan"), dtype=torch.float32, device="cuda")
+    jfa.fwd(plan, p.q, p.k, p.v, p.scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    return out, lse, plan
+
+
+def gpu_bwd(p: workloads.Problem, out, lse, plan: jfa.Plan):
+    dq = torch.full(p.q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    dk = torch.full(p.k.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    dv = torch.full(p.v.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    jfa.bwd(plan, p.q, p.k, p.v, out, p.dout, lse, p.scale, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    return dq, dk, dv
+
+
+def oracle_fwd(p: workloads.Problem):
+    return oracle.default().fwd(p.q, p.k, p.v, p.kv_offsets, p.q_offsets, p.B, p.H, p.Lq, p.D,
+                                p.scale)
+
+
+def oracle_bwd(p: workloads.Problem):
+    return oracle.default().bwd(p.q, p.k, p.v, p.dout, p.kv_offsets, p.q_offsets, p.B, p.H, p.Lq,
+                                p.D, p.scale)
+
+
+def check_fwd(O_gpu, L_gpu, O_ref, L_ref):
+    O = O_gpu.detach().cpu().double()
+    L = L_gpu.detach().cpu().double()
+    assert torch.isfinite(O).all(), "O has unwritten or non-finite entries"
+    fin = torch.isfinite(L_ref)
+    assert torch.equal(torch.isfinite(L), fin), "LSE finite pattern differs (unwritten rows?)"
+    assert (L[~fin] == L_ref[~fin]).all(), "rows without keys must have LSE = -inf"
+    err_o = (O - O_ref).abs().max().item() if O.numel() else 0.0
+    err_l = (L[fin] - L_ref[fin]).abs().max().item() if fin.any() else 0.0
+    assert err_o <= TOL_O, f"O max-abs error {err_o:.3e}"
+    assert err_l <= TOL_LSE, f"LSE max-abs error {err_l:.3e}"
+    return err_o, err_l
+
+
+def rel_l2(a, b) -> float:
+    a = a.detach().cpu().double()
+    b = b.detach().cpu().double()
+    den = b.norm().item()
+    num = (a - b).norm().item()
+    return num / den if den > 0 else num
+
+
+def check_grads(dq, dk, dv, rdq, rdk, rdv):
+    for name, g, r in (("dQ", dq, rdq), ("dK", dk, rdk), ("dV", dv, rdv)):
+        gc = g.detach().cpu().double()
+        assert torch.isfinite(gc).all(), f"{name} has unwritten or non-finite entries"
+        e = rel_l2(gc, r)
+        assert e <= TOL_GRAD, f"{name} relative L2 error {e:.3e}"

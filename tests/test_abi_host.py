@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/jfa.h declares, its schedule builder matches the reference
+builder bit for bit, and bad arguments are rejected before any launch."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import jagged_attention_gb300 as jfa
+import workloads
+from oracle import tiles as ref_tiles
+from tests.tiles_golden import load_cases
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    jfa.build()
+
+
+def test_exports_every_declared_function():
+    names = jfa.header_functions()
+    assert len(names) >= 9
+    L = jfa.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def _ref(qlen, klen, H, P, direction):
+    fn = ref_tiles.fwd_tiles if direction == 0 else ref_tiles.bwd_tiles
+    return fn(qlen, klen, H, 128, 128, P)
+
+
+@pytest.mark.parametrize("case", load_cases(), ids=lambda c: c["name"])
+def test_native_builder_matches_hand_worked(case):
+    kv = workloads.offsets_from_lengths(case["kv_lengths"])
+    ql = case["q_lengths"]
+    bcast = len(set(ql.tolist())) == 1 and case["name"].startswith("broadcast")
+    qo = None if bcast else workloads.offsets_from_lengths(ql)
+    Lq = int(ql[0]) if bcast else 0
+    for d, key in ((0, "fwd"), (1, "bwd")):
+        t, p = jfa.build_tiles(kv, qo, H=case["H"], Lq=Lq, num_ctas=case["num_ctas"], direction=d)
+        assert np.array_equal(t, case[key]) and np.array_equal(p, case[f"{key}_cta_ptr"])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_native_builder_matches_reference_random(seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 60))
+    H = int(rng.integers(1, 6))
+    klen = rng.integers(0, 1000, size=B)
+    klen[rng.random(B) < 0.15] = 0
+    P = int(rng.integers(1, 200))
+    kv = workloads.offsets_from_lengths(klen)
+    if seed % 2:
+        Lq = int(rng.integers(0, 400))
+        qlen, qo = np.full(B, Lq), None
+    else:
+        qlen = rng.integers(0, 700, size=B)
+        Lq, qo = 0, workloads.offsets_from_lengths(qlen)
+    for d in (0, 1):
+        t, p = jfa.build_tiles(kv, qo, H=H, Lq=Lq, num_ctas=P, direction=d)
+        rt, rp = _ref(qlen, klen, H, P, d)
+        assert np.array_equal(t, rt) and np.array_equal(p, rp)
+
+
+@pytest.mark.parametrize("name", sorted(workloads.WORKLOADS))
+def test_native_builder_matches_reference_on_workloads(name):
+    w = workloads.WORKLOADS[name]
+    klen = workloads.draw_lengths(w.lengths, w.B, 0)
+    kv = workloads.offsets_from_lengths(klen)
+    if w.mode == "broadcast":
+        qlen, qo, Lq = np.full(w.B, w.Lq), None, w.Lq
+    else:
+        qlen, qo, Lq = klen, kv, 0
+    for d in (0, 1):
+        t, p = jfa.build_tiles(kv, qo, H=w.H, Lq=Lq, num_ctas=152, direction=d)
+        rt, rp = _ref(qlen, klen, w.H, 152, d)
+        assert np.array_equal(t, rt) and np.array_equal(p, rp)
+
+
+def test_seed0_tile_counts():
+    # tile totals of the five workloads at seed 0
+    want = {"tiny_broadcast": (8, 8), "jagged_self": (624, 624), "gem_broadcast": (8192, 26028),
+            "skewed_broadcast": (32768, 89248), "block_diag": (294912, 294912)}
+    for name, (tf, tb) in want.items():
+        w = workloads.WORKLOADS[name]
+        kv = workloads.offsets_from_lengths(workloads.draw_lengths(w.lengths, w.B, 0))
+        qo = None if w.mode == "broadcast" else kv
+        assert jfa.build_tiles(kv, qo, H=w.H, Lq=w.Lq, num_ctas=152, direction=0)[0].shape[0] == tf
+        assert jfa.build_tiles(kv, qo, H=w.H, Lq=w.Lq, num_ctas=152, direction=1)[0].shape[0] == tb
+
+
+def _create(kv, qo, B, H, Lq, D, num_ctas=0):
+    L = jfa.lib()
+    h = ctypes.c_void_p()
+    kvp = None if kv is None else np.ascontiguousarray(kv, dtype=np.int32)
+    qop = None if qo is None else np.ascontiguousarray(qo, dtype=np.int32)
+    rc = L.jfa_plan_create(None if kvp is None else kvp.ctypes.data_as(jfa._i32p),
+                           None if qop is None else qop.ctypes.data_as(jfa._i32p),
+                           B, H, Lq, D, num_ctas, None, ctypes.byref(h))
+    return rc
+
+
+def test_rejects_bad_arguments_before_touching_the_device():
+    ok = [0, 5, 9]
+    assert _create(None, None, 2, 1, 4, 128) == 1                    # null offsets
+    assert _create(ok, None, 2, 0, 4, 128) == 1                      # H < 1
+    assert _create(ok, None, 2, 1, 4, 128, num_ctas=-1) == 1         # negative CTA count
+    assert _create(ok, None, 2, 1, 4, 96) == 2                       # D not 64/128
+    assert _create([1, 5, 9], None, 2, 1, 4, 128) == 3               # offsets[0] != 0
+    assert _create([0, 5, 3], None, 2, 1, 4, 128) == 3               # decreasing
+    assert _create(ok, [0, 2, 1], 2, 1, 0, 128) == 3                 # bad query offsets
+    assert _create(ok, None, 2, 1, -1, 128) == 1                     # negative Lq
+    L = jfa.lib()
+    T, P = ctypes.c_int(), ctypes.c_int()
+    kv = np.array([0, 4, 2], dtype=np.int32)
+    assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 0, None, None,
+                             ctypes.byref(T), ctypes.byref(P)) == 3
+    kv = np.array([0, 4, 6], dtype=np.int32)
+    assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 2, None, None,
+                             ctypes.byref(T), ctypes.byref(P)) == 1  # bad direction
+    assert L.jfa_fwd(None, None, None, None, 1.0, None, None, None) == 1
+    assert L.jfa_bwd(None, None, None, None, None, None, None, 1.0, None, None, None, None, 0,
+                     None) == 1
+    assert L.jfa_status_string(7) == b"device wait timed out"

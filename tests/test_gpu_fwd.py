@@ -1,0 +1,98 @@
+"""Forward parity on the GPU: the CUDA path through the C ABI against the fp64
+oracle, element by element, at sizes that span several tiles and a ragged
+tail, plus the edge cases (empty sequences, length 1, exact multiples of the
+tile, a single key block, long sequences, D = 64 and 128)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import jagged_attention_gb300 as jfa
+    jfa.build()
+
+
+def _run(p, num_ctas=0):
+    p = parity.to_cuda(p)
+    out, lse, plan = parity.gpu_fwd(p, parity.make_plan(p, num_ctas))
+    O_ref, L_ref = parity.oracle_fwd(p)
+    return parity.check_fwd(out, lse, O_ref, L_ref)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_broadcast_workload(seed):
+    _run(workloads.make_workload("tiny_broadcast", seed=seed))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_jagged_self_workload(seed):
+    _run(workloads.make_workload("jagged_self", seed=seed))
+
+
+EDGE_LENGTHS = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 0, 700]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_self_edge_lengths(D):
+    _run(workloads.make_problem(len(EDGE_LENGTHS), 2, D, "self", EDGE_LENGTHS, seed=3))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Lq", [1, 64, 128, 200, 256, 300])
+def test_broadcast_edge(D, Lq):
+    _run(workloads.make_problem(6, 3, D, "broadcast", [5, 0, 128, 129, 1000, 300], Lq=Lq, seed=4))
+
+
+def test_cross_lengths():
+    # jagged cross-attention: queries and keys with their own offsets
+    _run(workloads.make_problem(5, 2, 128, "self", [100, 300, 7, 0, 129],
+                                q_lengths=[130, 2, 0, 50, 256], seed=5))
+
+
+def test_long_sequences_and_few_ctas():
+    # many key blocks per tile and several tiles per CTA
+    _run(workloads.make_problem(3, 2, 128, "self", [3000, 1500, 129], seed=6), num_ctas=5)
+
+
+def test_single_cta():
+    _run(workloads.make_problem(5, 2, 64, "broadcast", [300, 10, 0, 700, 128], Lq=130, seed=7),
+         num_ctas=1)
+
+
+def test_single_key_block_matches_one_pass_softmax():
+    # with at most one key block the online softmax never rescales: compare
+    # with a one-pass softmax in fp32 on the same bf16 inputs
+    p = parity.to_cuda(workloads.make_problem(4, 2, 128, "self", [128, 77, 1, 100], seed=8))
+    out, lse, _ = parity.gpu_fwd(p)
+    off = p.kv_offsets
+    for b in range(p.B):
+        s, e = int(off[b]), int(off[b + 1])
+        for h in range(p.H):
+            q, k, v = p.q[s:e, h].float(), p.k[s:e, h].float(), p.v[s:e, h].float()
+            S = p.scale * q @ k.T
+            ref = torch.softmax(S, -1) @ v
+            assert (out[s:e, h].float() - ref).abs().max().item() < 1e-2
+            assert (lse[h, s:e] - torch.logsumexp(S, -1)).abs().max().item() < 1e-3
+
+
+def test_large_scores_rescale_path():
+    # scaled-up inputs make row maxima grow block to block, exercising the O rescale
+    p = workloads.make_problem(3, 2, 128, "self", [900, 400, 1300], seed=9)
+    ramp = torch.linspace(0.2, 3.0, p.k.shape[0])[:, None, None]
+    p.k = (p.k.float() * ramp).to(torch.bfloat16)
+    p.q = (p.q.float() * 2.0).to(torch.bfloat16)
+    _run(p)
+
+
+def test_repeated_calls_are_deterministic():
+    p = parity.to_cuda(workloads.make_workload("jagged_self", seed=2))
+    plan = parity.make_plan(p)
+    o1, l1, _ = parity.gpu_fwd(p, plan)
+    o2, l2, _ = parity.gpu_fwd(p, plan)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
