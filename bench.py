@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of the jagged attention hot path on GB300.
+
+One step = the whole path over one synthetic batch: forward (O, LSE), the
+backward pre-pass (Delta, dQ cleared) and the key/value-stationary backward
+(dQ reduced across the batch, dK, dV).  ``value`` is unpadded TFLOP/s
+(forward 4*D*H*sum_b Lq_b*Lk_b, backward 2.5x that) with inputs resident in
+HBM; ``e2e`` is the same metric through the public API with host buffers
+(plan build from host offsets, H2D of q/k/v/dO, D2H of O/LSE/dQ/dK/dV).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference      # the fp64 oracle on the host cores
+
+Under torchrun (N > 1) every rank runs an independent batch of the same
+shape (weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "gem_broadcast"
+METRIC = "jagged attn fwd/bwd TFLOP/s (unpadded FLOPs) and % of GB300 BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch from the committed ncu captures (profiles/), keyed by
+# kernel and workload, valid only while the kernel source hash matches.
+NCU_TRAFFIC = {}
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def pair_sum(prob: workloads.Problem) -> int:
+    """sum_b Lq_b * Lk_b (query-key pairs per head)."""
+    return int(np.sum(prob.q_lengths.astype(np.int64) * prob.kv_lengths.astype(np.int64)))
+
+
+def flops(prob, which: str) -> float:
+    base = 4.0 * prob.D * prob.H * pair_sum(prob)
+    return base if which == "fwd" else 2.5 * base
+
+
+def alg_bytes(prob, which: str) -> float:
+    """Algorithmic HBM bytes of one launch (each tensor read or written once)."""
+    row = prob.H * prob.D
+    q = prob.n_q_rows * row * 2
+    kv = prob.k.shape[0] * row * 2
+    o = prob.n_o_rows * row * 2
+    lse = prob.n_o_rows * prob.H * 4
+    if which == "fwd":
+        return q + 2 * kv + o + lse
+    if which == "pre":  # O and dO read, Delta written, dQ cleared
+        return 2 * o + lse + prob.n_q_rows * row * 4
+    # main: Q, K, V, dO, LSE, Delta read; dQ (fp32), dK, dV written
+    return q + 2 * kv + o + 2 * lse + prob.n_q_rows * row * 4 + 2 * kv
+
+
+def src_hash(name: str) -> str:
+    return hashlib.sha256((ROOT / "jagged_attention_gb300" / "csrc" / name).read_bytes()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        lines = [l for l in Path(self.out.name).read_text().splitlines() if l.strip()]
+        os.unlink(self.out.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, power) if p > 0.25 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "samples": len(sm), "power_w_max": max(power), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """The fp64 oracle (forward + backward), as it stands, on the first S
+    sequences of a batch; S is calibrated once so one run takes about
+    target_s seconds on the host cores."""
+
+    def __init__(self, prob, target_s: float):
+        import oracle
+
+        self.prob = prob
+        self.orc = oracle.default()
+        self.threads = self.orc.num_threads()
+        S, (fl, dt) = 1, self.run(1)
+        while dt < 0.5 * target_s and S < prob.B:
+            S = min(prob.B, max(S + 1, int(S * target_s / max(dt, 1e-3))))
+            fl, dt = self.run(S)
+        self.S = S
+
+    def run(self, S=None):
+        p = self.prob
+        S = self.S if S is None else S
+        kvo = workloads.offsets_from_lengths(p.kv_lengths[:S])
+        kv_rows = int(kvo[-1])
+        k, v = p.k[:kv_rows].cpu(), p.v[:kv_rows].cpu()
+        if p.mode == "broadcast":
+            q, qo, Lq = p.q.cpu(), None, p.Lq
+            dout = p.dout[:S * p.Lq].cpu()
+        else:
+            qo = workloads.offsets_from_lengths(p.q_lengths[:S])
+            q, dout, Lq = p.q[:int(qo[-1])].cpu(), p.dout[:int(qo[-1])].cpu(), 0
+        t0 = time.perf_counter()
+        self.orc.fwd(q, k, v, kvo, qo, S, p.H, Lq, p.D, p.scale)
+        self.orc.bwd(q, k, v, dout, kvo, qo, S, p.H, Lq, p.D, p.scale)
+        dt = time.perf_counter() - t0
+        fl = 3.5 * 4.0 * p.D * p.H * float(np.sum(p.q_lengths[:S] * p.kv_lengths[:S]))
+        return fl, dt
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    torch.manual_seed(0)
+    w = workloads.WORKLOADS[args.workload]
+    prob = workloads.make_workload(args.workload, seed=args.seed, device="cpu")
+    budget = min(30.0, 150.0 / max(1, args.steps + args.warmup))
+    sampler = OracleSample(prob, budget)
+    tfs, secs = [], []
+    for i in range(args.warmup + args.steps):
+        fl, dt = sampler.run()
+        if i >= args.warmup:
+            tfs.append(fl / dt / 1e12)
+            secs.append(dt)
+    S, threads = sampler.S, sampler.threads
+    value = statistics.median(tfs)
+    sample = (f"first {S} of {w.B} sequences of the seed-{args.seed} {args.workload} batch, "
+              f"fp64 forward + backward, {statistics.median(secs):.2f} s per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * statistics.median(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "D": w.D, "Lq": w.Lq,
+                   "lengths": list(map(str, w.lengths)), "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, dist):
+    import jagged_attention_gb300 as jfa
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        jfa.build()
+    if dist is not None:
+        dist.barrier()
+    jfa.lib()
+    w = workloads.WORKLOADS[args.workload]
+    prob = workloads.make_workload(args.workload, seed=args.seed + rank, device=dev)
+    plan = jfa.Plan(prob.kv_offsets, prob.q_offsets, H=prob.H, D=prob.D, Lq=prob.Lq)
+    out = torch.empty((prob.n_o_rows, prob.H, prob.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((prob.H, prob.n_o_rows), dtype=torch.float32, device=dev)
+    dq = torch.empty(prob.q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty_like(prob.k)
+    dv = torch.empty_like(prob.v)
+    ws = torch.empty(max(16, plan.workspace_bytes()), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        jfa.fwd(plan, prob.q, prob.k, prob.v, prob.scale, out=out, lse=lse, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        jfa.bwd_preprocess(plan, out, prob.dout, dq, dk, dv, ws, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        jfa.bwd_main(plan, prob.q, prob.k, prob.v, prob.dout, lse, prob.scale, dq, dk, dv, ws,
+                     stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    plan.device_status()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    status = plan.device_status()
+    total_ms = start.elapsed_time(stop)
+    k_fwd = sum(e[0].elapsed_time(e[1]) for e in evs)
+    k_pre = sum(e[1].elapsed_time(e[2]) for e in evs)
+    k_main = sum(e[2].elapsed_time(e[3]) for e in evs)
+    t = torch.tensor([total_ms, k_fwd, k_pre, k_main], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, k_fwd, k_pre, k_main = t.tolist()
+    ms_step = total_ms / args.steps
+
+    fl_step = flops(prob, "fwd") + flops(prob, "bwd")
+    value = world * fl_step / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ------------------
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, prob, dev, stream, jfa)
+        if dist is not None:
+            tt = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e["ms_per_step"] = tt.item()
+        e2e["value"] = world * fl_step / (e2e["ms_per_step"] * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+
+    pk, pk_kind = peaks()
+    tf_peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    bw_peak = pk["hbm_gbs"]
+    per_kernel = {
+        "jfa_fwd_kernel": {"ms": k_fwd / args.steps, "flops": flops(prob, "fwd"),
+                           "bytes": alg_bytes(prob, "fwd"), "src": "fwd.cu"},
+        "bwd_preprocess": {"ms": k_pre / args.steps, "flops": 0.0, "bytes": alg_bytes(prob, "pre"),
+                           "src": "bwd.cu"},
+        "jfa_bwd_kernel": {"ms": k_main / args.steps, "flops": flops(prob, "bwd"),
+                           "bytes": alg_bytes(prob, "main"), "src": "bwd.cu"},
+    }
+    for name, d in per_kernel.items():
+        s = d["ms"] * 1e-3
+        d["tflops"] = d["flops"] / s / 1e12 if d["flops"] else 0.0
+        d["gbs"] = d["bytes"] / s / 1e9
+        d["tensor_frac"] = d["tflops"] / tf_peak
+        d["hbm_frac"] = d["gbs"] / bw_peak
+    dom_name = max(("jfa_fwd_kernel", "jfa_bwd_kernel"), key=lambda n: per_kernel[n]["ms"])
+    dom = per_kernel[dom_name]
+    ridge = tf_peak * 1e12 / (bw_peak * 1e9)
+    ai = dom["flops"] / dom["bytes"]
+    key = f"{dom_name}:{args.workload}"
+    tr = NCU_TRAFFIC.get(key)
+    traffic = tr["bytes"] if tr and tr.get("src_hash") == src_hash(dom["src"]) else None
+    if ai >= ridge:
+        roof = {"bound": "tensor", "achieved": dom["tflops"], "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": dom["tflops"] / tf_peak}
+    else:
+        roof = {"bound": "hbm", "achieved": dom["gbs"], "peak": bw_peak, "unit": "GB/s",
+                "frac": dom["gbs"] / bw_peak}
+    roof.update({"traffic": traffic, "kernel": dom_name, "peak_source": f"{pk_kind} "
+                 f"({'bf16 sustained' if roof['bound'] == 'tensor' else 'hbm copy'})",
+                 "arith_intensity": ai, "ridge": ridge,
+                 "tensor_frac": dom["tensor_frac"], "hbm_frac": dom["hbm_frac"]})
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        sampler = OracleSample(prob, args.cpu_seconds)
+        fl, secs = sampler.run()
+        cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": sampler.threads,
+               "kind": "oracle",
+               "sample": f"first {sampler.S} of {w.B} sequences of the same batch, fp64 forward "
+                         f"+ backward, {secs:.1f} s"}
+
+    kv_gb = 2 * prob.k.numel() * 2 / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "D": w.D, "Lq": w.Lq,
+                   "mode": w.mode, "lengths": list(map(str, w.lengths)), "seed": args.seed,
+                   "sum_kv_tokens": int(prob.kv_offsets[-1]),
+                   "l2": f"inputs larger than L2 (K+V {kv_gb:.2f} GB per step), no flush",
+                   "parallelism": f"dp{world} (independent batches)"},
+        "fwd_tflops": per_kernel["jfa_fwd_kernel"]["tflops"],
+        "bwd_tflops": flops(prob, "bwd") / ((k_pre + k_main) / args.steps * 1e-3) / 1e12,
+        "pct_bf16_peak": {"fwd": 100 * per_kernel["jfa_fwd_kernel"]["tensor_frac"],
+                          "bwd_main": 100 * per_kernel["jfa_bwd_kernel"]["tensor_frac"],
+                          "step": 100 * (value / world) / tf_peak},
+        "kernels": per_kernel,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": None if e2e is None else {k: e2e[k] for k in
+                                          ("value", "unit", "h2d_bytes_per_step",
+                                           "d2h_bytes_per_step", "ms_per_step")},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, prob, dev, stream, jfa):
+    """Public-API step with host buffers: plan from host offsets, H2D inputs from
+    pinned memory, forward + backward, D2H of every output."""
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv, hdo = pin(prob.q), pin(prob.k), pin(prob.v), pin(prob.dout)
+    dq_ = torch.empty_like(prob.q)
+    dk_ = torch.empty_like(prob.k)
+    dv_ = torch.empty_like(prob.v)
+    ddo = torch.empty_like(prob.dout)
+    ho = torch.empty((prob.n_o_rows, prob.H, prob.D), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((prob.H, prob.n_o_rows), dtype=torch.float32).pin_memory()
+    hdq = torch.empty(prob.q.shape, dtype=torch.float32).pin_memory()
+    hdk = torch.empty(prob.k.shape, dtype=torch.bfloat16).pin_memory()
+    hdv = torch.empty(prob.v.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * (prob.B + 1) * (
+        1 if prob.q_offsets is None else 2)
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+
+    def step():
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        ddo.copy_(hdo, non_blocking=True)
+        plan = jfa.Plan(prob.kv_offsets, prob.q_offsets, H=prob.H, D=prob.D, Lq=prob.Lq,
+                        stream=stream)
+        o, l = jfa.fwd(plan, dq_, dk_, dv_, prob.scale, stream=stream)
+        g = jfa.bwd(plan, dq_, dk_, dv_, o, ddo, l, prob.scale, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(l, non_blocking=True)
+        hdq.copy_(g[0], non_blocking=True)
+        hdk.copy_(g[1], non_blocking=True)
+        hdv.copy_(g[2], non_blocking=True)
+        torch.cuda.synchronize()
+        plan.close()
+
+    n = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1000 / n
+    return {"unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist_.init_process_group(backend)
+        dist = dist_
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -136,6 +136,20 @@ int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const 
             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The two stages jfa_bwd runs, for callers that schedule them separately
+ * (same arguments and rules as jfa_bwd).
+ * jfa_bwd_preprocess: Delta (into workspace) from out and dout, clears dq,
+ *   and zeroes dk / dv rows of sequences that have keys but no queries.
+ * jfa_bwd_main: the key/value-stationary pass; needs the workspace written by
+ *   jfa_bwd_preprocess (stream order) and the cleared dq.
+ */
+int jfa_bwd_preprocess(jfa_plan_t plan, const void* out, const void* dout, float* dq, void* dk,
+                       void* dv, void* workspace, size_t workspace_bytes, void* stream);
+int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, const void* dout,
+                 const float* lse, float scale, float* dq, void* dk, void* dv,
+                 const void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Read the plan's device status word (synchronises `stream`), then clear it.
  * Returns JFA_ERR_DEVICE_TIMEOUT when a kernel recorded a wait that ran out,
  * JFA_OK otherwise; *raw (optional) receives the raw word.

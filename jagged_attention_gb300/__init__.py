@@ -68,11 +68,15 @@ def lib() -> ctypes.CDLL:
             L.jfa_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.jfa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
                                   _vp, ctypes.c_size_t, _vp]
+            L.jfa_bwd_preprocess.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+            L.jfa_bwd_main.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
+                                       _vp, ctypes.c_size_t, _vp]
             L.jfa_plan_device_status.argtypes = [_vp, _vp, _ip]
             L.jfa_status_string.argtypes = [ctypes.c_int]
             L.jfa_status_string.restype = ctypes.c_char_p
             for name in ("jfa_plan_create", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
-                         "jfa_fwd", "jfa_bwd", "jfa_plan_device_status"):
+                         "jfa_fwd", "jfa_bwd", "jfa_bwd_preprocess", "jfa_bwd_main",
+                         "jfa_plan_device_status"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -230,3 +234,23 @@ def header_functions() -> list[str]:
     text = HEADER.read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(jfa_[a-z_0-9]+)\s*\(", text)))
+
+
+def bwd_preprocess(plan: Plan, out, dout, dq, dk, dv, workspace, stream=None):
+    """Delta into ``workspace``, dq cleared, dK/dV of query-less sequences zeroed."""
+    _check(lib().jfa_bwd_preprocess(plan.handle, _dev(out, "out", torch.bfloat16),
+                                    _dev(dout, "dout", torch.bfloat16), _dev(dq, "dq", torch.float32),
+                                    _dev(dk, "dk", torch.bfloat16), _dev(dv, "dv", torch.bfloat16),
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)), "jfa_bwd_preprocess")
+
+
+def bwd_main(plan: Plan, q, k, v, dout, lse, scale: float, dq, dk, dv, workspace, stream=None):
+    """The key/value-stationary backward pass (after bwd_preprocess on the same stream)."""
+    _check(lib().jfa_bwd_main(plan.handle, _dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16),
+                              _dev(v, "v", torch.bfloat16), _dev(dout, "dout", torch.bfloat16),
+                              _dev(lse, "lse", torch.float32), float(scale),
+                              _dev(dq, "dq", torch.float32), _dev(dk, "dk", torch.bfloat16),
+                              _dev(dv, "dv", torch.bfloat16), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "jfa_bwd_main")

@@ -273,22 +273,19 @@ size_t jfa_bwd_workspace_bytes(jfa_plan_t plan) {
   return align_up(static_cast<size_t>(plan->n_o) * plan->H * sizeof(float), 256);
 }
 
-int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const void* out,
-            const void* dout, const float* lse, float scale, float* dq, void* dk, void* dv,
-            void* workspace, size_t workspace_bytes, void* stream) {
-  if (!plan || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
-  if ((plan->n_q > 0 && (!q || !dq)) || (plan->n_kv > 0 && (!k || !v || !dk || !dv)) ||
-      (plan->n_o > 0 && (!out || !dout || !lse)))
+int jfa_bwd_preprocess(jfa_plan_t plan, const void* out, const void* dout, float* dq, void* dk,
+                       void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan) return JFA_ERR_INVALID_ARG;
+  if ((plan->n_q > 0 && !dq) || (plan->n_kv > 0 && (!dk || !dv)) ||
+      (plan->n_o > 0 && (!out || !dout)))
     return JFA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+  if (!aligned16(out) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(workspace))
     return JFA_ERR_ALIGNMENT;
-  const size_t need = jfa_bwd_workspace_bytes(plan);
-  if (plan->n_o > 0 && (!workspace || workspace_bytes < need)) return JFA_ERR_WORKSPACE;
+  if (plan->n_o > 0 && (!workspace || workspace_bytes < jfa_bwd_workspace_bytes(plan)))
+    return JFA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t cols = int64_t(plan->H) * plan->D;
-  float* delta = static_cast<float*>(workspace);
-
   // dQ is reduce-added by the key/value tiles: start from zero
   if (plan->n_q > 0 &&
       cudaMemsetAsync(dq, 0, static_cast<size_t>(plan->n_q) * cols * sizeof(float), s) != cudaSuccess)
@@ -301,11 +298,27 @@ int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const 
         cudaMemsetAsync(static_cast<uint8_t*>(dv) + off, 0, len, s) != cudaSuccess)
       return JFA_ERR_CUDA;
   }
-  if (plan->bwd.P == 0) return JFA_OK;
+  if (plan->bwd.P == 0 || plan->n_o == 0) return JFA_OK;
   cudaError_t e = jfa::launch_delta(static_cast<const uint16_t*>(out),
-                                    static_cast<const uint16_t*>(dout), delta, plan->n_o, plan->H,
-                                    plan->D, s);
-  if (e != cudaSuccess) return JFA_ERR_CUDA;
+                                    static_cast<const uint16_t*>(dout),
+                                    static_cast<float*>(workspace), plan->n_o, plan->H, plan->D, s);
+  return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, const void* dout,
+                 const float* lse, float scale, float* dq, void* dk, void* dv,
+                 const void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if ((plan->n_q > 0 && (!q || !dq)) || (plan->n_kv > 0 && (!k || !v || !dk || !dv)) ||
+      (plan->n_o > 0 && (!dout || !lse)))
+    return JFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return JFA_ERR_ALIGNMENT;
+  if (plan->n_o > 0 && (!workspace || workspace_bytes < jfa_bwd_workspace_bytes(plan)))
+    return JFA_ERR_WORKSPACE;
+  if (plan->bwd.P == 0) return JFA_OK;
+  const int64_t cols = int64_t(plan->H) * plan->D;
   CUtensorMap qm, km, vm, dom;
   if (make_map(&qm, q, plan->n_q, cols) || make_map(&km, k, plan->n_kv, cols) ||
       make_map(&vm, v, plan->n_kv, cols) || make_map(&dom, dout, plan->n_o, cols))
@@ -317,14 +330,23 @@ int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const 
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.lse = lse;
-  a.delta = delta;
+  a.delta = static_cast<const float*>(workspace);
   a.dq = dq;
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
   a.status = plan->d_status;
-  e = jfa::launch_bwd(a, qm, km, vm, dom, plan->bwd.P, s);
-  if (e == cudaErrorNotSupported) return JFA_ERR_UNSUPPORTED;
+  cudaError_t e = jfa::launch_bwd(a, qm, km, vm, dom, plan->bwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const void* out,
+            const void* dout, const float* lse, float scale, float* dq, void* dk, void* dv,
+            void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  int rc = jfa_bwd_preprocess(plan, out, dout, dq, dk, dv, workspace, workspace_bytes, stream);
+  if (rc != JFA_OK) return rc;
+  return jfa_bwd_main(plan, q, k, v, dout, lse, scale, dq, dk, dv, workspace, workspace_bytes,
+                      stream);
 }
 
 }  // extern "C"

@@ -40,6 +40,457 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+
+// ===========================================================================
+// Key/value-stationary backward.
+//
+// Tile (b, h, n): the 128 keys K_n and values V_n stay in shared memory while
+// the CTA walks the sequence's query blocks m (broadcast mode: the blocks of
+// the one dense Q).  Per query block, with S = Q K^T unscaled and
+// c = scale*log2(e):
+//   S^T   = K_n Q_m^T                  tcgen05.mma -> TMEM (kv rows = lanes)
+//   dP^T  = V_n dO_m^T                 tcgen05.mma -> TMEM
+//   P^T   = exp2(c S^T - LSE*log2 e)   WG0, written back to TMEM as bf16
+//   dS^T  = P^T o (dP^T - Delta)       WG0, written to swizzled shared memory
+//   dV   += P^T dO_m                   A = P^T from TMEM
+//   dK   += dS^T Q_m                   A = dS^T, K-major view
+//   dQ_m  = dS K_n                     A = the same dS^T buffer, M-major view
+// dQ_m is drained by WG1 (TMEM -> registers -> fp32 vector reduce-add into
+// dq; in broadcast mode every sequence's tiles add into the same rows: the
+// cross-batch reduction of the GEM page, "GEM's sequences do not fit a fixed
+// grid").  The TMEM slice holding dQ_m is released as soon as it sits in
+// registers, before the global reductions (the pages' early TMEM release).
+// At the end of a tile WG1 writes dV and scale*dK in bf16.
+//
+//   warps 0-3  WG0: P^T and dS^T (thread = key row)
+//   warps 4-7  WG1: dQ drain (thread = query row), dK / dV epilogue
+//   warp 8     TMA producer: K_n, V_n per tile; Q_m, dO_m double-buffered
+//   warp 9     tcgen05.mma issuer, TMEM owner
+// TMEM: S^T [0,128) (P^T bf16 pairs in its first 64 columns), dP^T [128,256)
+// (dQ_m reuses it), dV [256, 256+D), dK [256+D, 256+2D).
+// ===========================================================================
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = 128 * 128;       // [128 rows x 64 bf16]
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;        // 2 stages
+  static constexpr int kOffDO = 4 * kTileBytes;       // 2 stages
+  static constexpr int kOffDS = 6 * kTileBytes;       // dS^T [128 keys x 128 queries] bf16
+  static constexpr int kOffLse = kOffDS + 32768;      // 128 LSE*log2(e), 128 Delta (fp32)
+  static constexpr int kOffBar = kOffLse + 1024;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kColDV = 256;
+  static constexpr uint32_t kColDK = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 320;
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;
+};
+
+struct BwdBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full;
+  uint64_t dv_done, ds_empty;
+  uint64_t dq_full, dq_empty;
+  uint64_t dkv_full, dkv_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct BTile {
+  int b, h, n, qblocks;
+};
+__device__ __forceinline__ BTile load_btile(const int32_t* tiles, int i) {
+  const int4 t = __ldg(reinterpret_cast<const int4*>(tiles) + i);
+  return {t.x, t.y, t.z, t.w};
+}
+
+__device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, const Abort& ab) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
+}
+__device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void bwd_producer(const BwdArgs& a, const CUtensorMap* q_map, const CUtensorMap* k_map,
+                             const CUtensorMap* v_map, const CUtensorMap* do_map, uint32_t sbase,
+                             BwdBars& bars, const Abort& ab, int t_begin, int t_end) {
+  using C = BwdCfg<D>;
+  tma_prefetch_desc(q_map);
+  tma_prefetch_desc(k_map);
+  tma_prefetch_desc(v_map);
+  tma_prefetch_desc(do_map);
+  uint32_t ntile = 0, nq = 0;  // K/V and Q/dO stage loads issued
+  bool ok = true;
+  for (int i = t_begin; i < t_end && ok; ++i) {
+    const BTile t = load_btile(a.tiles, i);
+    const int x0 = t.h * D;
+    const int k_row0 = a.pb.kv_off[t.b] + t.n * 128;
+    const int q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
+    const int o_base = a.pb.q_off ? a.pb.q_off[t.b] : t.b * a.pb.Lq;
+    ok = mbar_wait(smem_u32(&bars.kv_empty), (ntile & 1) ^ 1, ab);
+    if (!ok) break;
+    mbar_arrive_expect_tx(smem_u32(&bars.kv_full), 2 * C::kTileBytes);
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c) {
+      tma_load_2d(sbase + C::kOffK + c * C::kChunkBytes, k_map, smem_u32(&bars.kv_full), x0 + c * 64, k_row0);
+      tma_load_2d(sbase + C::kOffV + c * C::kChunkBytes, v_map, smem_u32(&bars.kv_full), x0 + c * 64, k_row0);
+    }
+    ++ntile;
+    for (int m = 0; m < t.qblocks && ok; ++m) {
+      const uint32_t qs = nq & 1, ph = (nq >> 1) & 1;
+      ok = mbar_wait(smem_u32(&bars.q_empty[qs]), ph ^ 1, ab);
+      if (!ok) break;
+      mbar_arrive_expect_tx(smem_u32(&bars.q_full[qs]), 2 * C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_2d(sbase + C::kOffQ + qs * C::kTileBytes + c * C::kChunkBytes, q_map,
+                    smem_u32(&bars.q_full[qs]), x0 + c * 64, q_base + m * 128);
+        tma_load_2d(sbase + C::kOffDO + qs * C::kTileBytes + c * C::kChunkBytes, do_map,
+                    smem_u32(&bars.q_full[qs]), x0 + c * 64, o_base + m * 128);
+      }
+      ++nq;
+    }
+  }
+  // let every issued copy land before the CTA may exit
+  if (ntile > 0) drain_wait_b(smem_u32(&bars.kv_full), (ntile - 1) & 1);
+  for (uint32_t qs = 0; qs < 2 && qs < nq; ++qs) {
+    const uint32_t last = nq - 1 - ((nq - 1 - qs) & 1);
+    drain_wait_b(smem_u32(&bars.q_full[qs]), (last >> 1) & 1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars& bars,
+                        const Abort& ab, int t_begin, int t_end) {
+  using C = BwdCfg<D>;
+  constexpr uint32_t id_sdp = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+  constexpr uint32_t id_kmaj = idesc_bf16_f32(128, D, false, true);    // dV (A in TMEM), dK
+  constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);       // dQ: A = dS (M-major)
+  const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sDS = sbase + C::kOffDS;
+  uint32_t gm = 0, tt = 0;
+  bool ok = true;
+  for (int i = t_begin; i < t_end && ok; ++i) {
+    const BTile t = load_btile(a.tiles, i);
+    for (int m = 0; m < t.qblocks && ok; ++m, ++gm) {
+      const uint32_t qs = gm & 1;
+      const uint32_t sQ = sbase + C::kOffQ + qs * C::kTileBytes;
+      const uint32_t sDO = sbase + C::kOffDO + qs * C::kTileBytes;
+      ok = mbar_wait(smem_u32(&bars.q_full[qs]), (gm >> 1) & 1, ab);
+      if (ok && m == 0) ok = mbar_wait(smem_u32(&bars.kv_full), tt & 1, ab);
+      // S^T region is free once the previous step's dV (which read P^T there) completed
+      if (ok) ok = mbar_wait(smem_u32(&bars.dv_done), (gm & 1) ^ 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+        mma_bf16_ss(tmem + C::kColS, smem_desc_sw128(sK + koff, 16, 1024),
+                    smem_desc_sw128(sQ + koff, 16, 1024), id_sdp, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&bars.s_full));
+      // dP^T region is free once WG1 has the previous dQ in registers
+      ok = mbar_wait(smem_u32(&bars.dq_empty), (gm & 1) ^ 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+        mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sV + koff, 16, 1024),
+                    smem_desc_sw128(sDO + koff, 16, 1024), id_sdp, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&bars.dp_full));
+      if (m == 0) ok = mbar_wait(smem_u32(&bars.dkv_empty), (tt & 1) ^ 1, ab);
+      if (ok) ok = mbar_wait(smem_u32(&bars.p_full), gm & 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_m, K = 128 queries
+        mma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+                    smem_desc_sw128(sDO + kk * 2048, C::kChunkBytes, 1024), id_kmaj,
+                    (m > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(smem_u32(&bars.dv_done));
+      ok = mbar_wait(smem_u32(&bars.ds_full), gm & 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_m
+        mma_bf16_ss(tmem + C::kColDK,
+                    smem_desc_sw128(sDS + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024),
+                    smem_desc_sw128(sQ + kk * 2048, C::kChunkBytes, 1024), id_kmaj,
+                    (m > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // dQ_m = dS K_n, K = 128 keys
+        mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sDS + kk * 2048, C::kChunkBytes, 1024),
+                    smem_desc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), id_dq,
+                    kk > 0 ? 1u : 0u);
+      mma_commit(smem_u32(&bars.dq_full));
+      mma_commit(smem_u32(&bars.ds_empty));
+      mma_commit(smem_u32(&bars.q_empty[qs]));
+      if (m == t.qblocks - 1) {
+        mma_commit(smem_u32(&bars.dkv_full));
+        mma_commit(smem_u32(&bars.kv_empty));
+      }
+    }
+    ++tt;
+  }
+  mma_commit(smem_u32(&bars.drain));
+  drain_wait_b(smem_u32(&bars.drain), 0);
+}
+
+// ---------------------------------------------------------------------------
+// WG0: P^T and dS^T, one thread per key row (TMEM lane)
+template <int D>
+__device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uint32_t tmem, BwdBars& bars,
+                            const Abort& ab, int t_begin, int t_end) {
+  using C = BwdCfg<D>;
+  const int r = threadIdx.x;  // 0..127
+  const int warp = r >> 5;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  float* lse2 = reinterpret_cast<float*>(smem + C::kOffLse);  // 128 LSE*log2(e), then 128 Delta
+  float* dlt = lse2 + 128;
+  uint32_t gm = 0;
+  for (int i = t_begin; i < t_end; ++i) {
+    const BTile t = load_btile(a.tiles, i);
+    const int64_t klen = a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b];
+    const bool kv_ok = int64_t(t.n) * 128 + r < klen;
+    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + 1] - a.pb.q_off[t.b]) : a.pb.Lq;
+    const int64_t o_base = a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq;
+    for (int m = 0; m < t.qblocks; ++m, ++gm) {
+      // per-query LSE (log2 units) and Delta of this block, masked past the sequence
+      named_bar_sync(1, 128);  // everyone is done with the previous block's values
+      {
+        const bool q_ok = int64_t(m) * 128 + r < qlen;
+        const int64_t idx = int64_t(t.h) * a.pb.n_o + o_base + m * 128 + r;
+        lse2[r] = q_ok ? a.lse[idx] * 1.4426950408889634f : INFINITY;
+        dlt[r] = q_ok ? a.delta[idx] : 0.0f;
+      }
+      named_bar_sync(1, 128);
+
+      if (!warp_wait_b(smem_u32(&bars.s_full), gm & 1, ab)) return;
+      tc_fence_after();
+      uint32_t p[64];  // P^T row, bf16 pairs
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_x32(tl + C::kColS + c * 32, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = c * 32 + 2 * e;
+          float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, -lse2[j]));
+          float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, -lse2[j + 1]));
+          if (!kv_ok) p0 = p1 = 0.0f;
+          p[c * 16 + e] = pack_bf16x2(p0, p1);
+        }
+      }
+      {
+        uint32_t lo[32], hi[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          lo[e] = p[e];
+          hi[e] = p[32 + e];
+        }
+        tmem_st_x32(tl + C::kColS, lo);
+        tmem_st_x32(tl + C::kColS + 32, hi);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.p_full));
+
+      if (!warp_wait_b(smem_u32(&bars.dp_full), gm & 1, ab)) return;
+      // the dS^T buffer is free once the previous step's dK and dQ products completed
+      if (!warp_wait_b(smem_u32(&bars.ds_empty), (gm & 1) ^ 1, ab)) return;
+      tc_fence_after();
+      const uint32_t sDS = sbase + C::kOffDS;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_x32(tl + C::kColDP + c * 32, v);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = c * 32 + 2 * e;
+          const uint32_t pp = p[c * 16 + e];
+          const float d0 = __uint_as_float(pp << 16) * (__uint_as_float(v[2 * e]) - dlt[j]);
+          const float d1 = __uint_as_float(pp & 0xffff0000u) * (__uint_as_float(v[2 * e + 1]) - dlt[j + 1]);
+          w[e] = pack_bf16x2(d0, d1);
+        }
+        // query columns 32c..32c+31 = 128-byte chunk c/2, 16-byte units (c%2)*4 .. +3
+        const uint32_t base = sDS + (c >> 1) * C::kChunkBytes;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(base + sw128_offset(r, (c & 1) * 4 + q4), w[4 * q4], w[4 * q4 + 1],
+                       w[4 * q4 + 2], w[4 * q4 + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.ds_full));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// WG1: dQ drain (thread = query row) and the dK / dV epilogue (thread = key row)
+template <int D>
+__device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const Abort& ab,
+                          int t_begin, int t_end) {
+  using C = BwdCfg<D>;
+  const int r = threadIdx.x - 128;  // 0..127
+  const int warp = r >> 5;          // TMEM lane quarter: warps 4-7 -> 0-3
+  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int H = a.pb.H;
+  uint32_t gm = 0, tt = 0;
+  for (int i = t_begin; i < t_end; ++i) {
+    const BTile t = load_btile(a.tiles, i);
+    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + 1] - a.pb.q_off[t.b]) : a.pb.Lq;
+    const int64_t q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
+    for (int m = 0; m < t.qblocks; ++m, ++gm) {
+      if (!warp_wait_b(smem_u32(&bars.dq_full), gm & 1, ab)) return;
+      tc_fence_after();
+      uint32_t v[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t w[32];
+        tmem_ld_x32(tl + C::kColDP + c * 32, w);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[c * 32 + e] = w[e];
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.dq_empty));  // TMEM released before the global reductions
+      if (int64_t(m) * 128 + r < qlen) {
+        float4* dst = reinterpret_cast<float4*>(a.dq + ((q_base + m * 128 + r) * H + t.h) * D);
+#pragma unroll
+        for (int e = 0; e < D / 4; ++e)
+          atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]) * a.scale,
+                                         __uint_as_float(v[4 * e + 1]) * a.scale,
+                                         __uint_as_float(v[4 * e + 2]) * a.scale,
+                                         __uint_as_float(v[4 * e + 3]) * a.scale));
+      }
+    }
+    // tile done: dV and scale * dK rows in bf16
+    if (!warp_wait_b(smem_u32(&bars.dkv_full), tt & 1, ab)) return;
+    tc_fence_after();
+    const int64_t klen = a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b];
+    const bool kv_ok = int64_t(t.n) * 128 + r < klen;
+    const int64_t krow = int64_t(a.pb.kv_off[t.b]) + t.n * 128 + r;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+      const float mul = which == 0 ? 1.0f : a.scale;
+      uint16_t* dst_row = (which == 0 ? a.dv : a.dk) + (krow * H + t.h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t w[32];
+        tmem_ld_x32(tl + col + c * 32, w);
+        if (kv_ok) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(w[2 * e]) * mul, __uint_as_float(w[2 * e + 1]) * mul);
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&bars.dkv_empty));
+    ++tt;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    jfa_bwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+                   const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap do_map,
+                   const BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  BwdBars& bars = *reinterpret_cast<BwdBars*>(smem + C::kOffBar);
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t_begin = a.cta_ptr[blockIdx.x], t_end = a.cta_ptr[blockIdx.x + 1];
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars.kv_full), 1);
+    mbar_init(smem_u32(&bars.kv_empty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars.q_full[s]), 1);
+      mbar_init(smem_u32(&bars.q_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars.s_full), 1);
+    mbar_init(smem_u32(&bars.dp_full), 1);
+    mbar_init(smem_u32(&bars.p_full), 128);
+    mbar_init(smem_u32(&bars.ds_full), 128);
+    mbar_init(smem_u32(&bars.dv_done), 1);
+    mbar_init(smem_u32(&bars.ds_empty), 1);
+    mbar_init(smem_u32(&bars.dq_full), 1);
+    mbar_init(smem_u32(&bars.dq_empty), 128);
+    mbar_init(smem_u32(&bars.dkv_full), 1);
+    mbar_init(smem_u32(&bars.dkv_empty), 128);
+    mbar_init(smem_u32(&bars.drain), 1);
+    bars.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(smem_u32(&bars.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const Abort ab{&bars.abort_flag, a.status};
+  if (warp < 4) {
+    bwd_softmax<D>(a, smem, sbase, tmem, bars, ab, t_begin, t_end);
+  } else if (warp < 8) {
+    bwd_drain<D>(a, tmem, bars, ab, t_begin, t_end);
+  } else if (warp == C::kProducerWarp) {
+    if (lane == 0) bwd_producer<D>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, t_begin, t_end);
+    __syncwarp();
+  } else {
+    if (lane == 0) bwd_mma<D>(a, sbase, tmem, bars, ab, t_begin, t_end);
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
+                         const CUtensorMap& v, const CUtensorMap& dO, int grid, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  static_assert(C::kSmemBytes <= 232448, "shared memory budget");
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(jfa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  jfa_bwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta, int64_t n_o,
@@ -51,9 +502,15 @@ cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const BwdArgs&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                       const CUtensorMap&, int, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
 
+}  // namespace jfa
+
+namespace jfa {
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                       const CUtensorMap& v_map, const CUtensorMap& do_map, int grid,
+                       cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  if (a.pb.D == 128) return launch_bwd_d<128>(a, q_map, k_map, v_map, do_map, grid, stream);
+  return launch_bwd_d<64>(a, q_map, k_map, v_map, do_map, grid, stream);
+}
 }  // namespace jfa

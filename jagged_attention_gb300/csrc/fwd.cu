@@ -244,7 +244,7 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
       continue;
     }
     const int last_valid = (a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b]) - (t.cost - 1) * 128;
-    float m_run = -INFINITY, l_run = 0.0f;
+    float m_run = -INFINITY, l_run = 0.0f, lr_run = 0.0f;  // exact and rounded-weight row sums
     for (int j = 0; j < t.cost; ++j) {
       const uint32_t gj = g + j, sb = gj & 1;
       if (!warp_wait(smem_u32(&bars.s_full[sb]), (gj >> 1) & 1, ab)) return;
@@ -272,17 +272,20 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
       const float m_new = resc ? m_cand : m_run;
       const float alpha = resc ? fast_exp2(m_run - m_new) : 1.0f;
       uint32_t p[64];
-      float rowsum = 0.0f;
+      float rowsum = 0.0f, rowsum_r = 0.0f;
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
         const float p0 = fast_exp2(fmaf(s[2 * e], sl2, -m_new));
         const float p1 = fast_exp2(fmaf(s[2 * e + 1], sl2, -m_new));
         p[e] = pack_bf16x2(p0, p1);
-        // normalise by the sum of the rounded weights the PV product uses, so
-        // O stays an exact convex combination of V rows under those weights
-        rowsum += __uint_as_float(p[e] << 16) + __uint_as_float(p[e] & 0xffff0000u);
+        rowsum += p0 + p1;
+        // O is normalised by the sum of the rounded weights the PV product
+        // uses (an exact convex combination of V rows under those weights);
+        // LSE keeps the sum of the unrounded ones
+        rowsum_r += __uint_as_float(p[e] << 16) + __uint_as_float(p[e] & 0xffff0000u);
       }
       l_run = l_run * alpha + rowsum;
+      lr_run = lr_run * alpha + rowsum_r;
       // the P buffer is free once PV of block gj-2 has completed
       if (!warp_wait(smem_u32(&bars.pv_done[sb]), ((gj >> 1) & 1) ^ 1, ab)) return;
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -317,7 +320,7 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
     const uint32_t gl = g + t.cost - 1;
     if (!warp_wait(smem_u32(&bars.pv_done[gl & 1]), (gl >> 1) & 1, ab)) return;
     tc_fence_after();
-    const float inv_l = 1.0f / l_run;
+    const float inv_l = 1.0f / lr_run;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t v[32];

@@ -87,6 +87,9 @@ def test_large_scores_rescale_path():
     ramp = torch.linspace(0.2, 3.0, p.k.shape[0])[:, None, None]
     p.k = (p.k.float() * ramp).to(torch.bfloat16)
     p.q = (p.q.float() * 2.0).to(torch.bfloat16)
+    # peaky rows put O close to single V rows; halving V keeps |O| < 2 so the
+    # bf16 output rounding (half an ulp) stays below 4e-3 of the 1e-2 budget
+    p.v = (p.v.float() * 0.5).to(torch.bfloat16)
     _run(p)
 
 
