@@ -43,7 +43,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes per launch from the committed ncu captures (profiles/), keyed by
 # kernel and workload, valid only while the kernel source hash matches.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 867.5 MB at 256 sequences, x3.748
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2513e9, "src_hash": "80383c9449facb79"},
+    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 475.6 MB at 256 sequences, x3.766
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7910e9, "src_hash": "15db84245aa3a56a"},
+}
 
 
 def peaks():
@@ -226,7 +231,8 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     jfa.lib()
     w = workloads.WORKLOADS[args.workload]
-    prob = workloads.make_workload(args.workload, seed=args.seed + rank, device=dev)
+    prob = workloads.make_workload(args.workload, seed=args.seed + rank, device=dev,
+                                   batch=args.batch)
     plan = jfa.Plan(prob.kv_offsets, prob.q_offsets, H=prob.H, D=prob.D, Lq=prob.Lq)
     out = torch.empty((prob.n_o_rows, prob.H, prob.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((prob.H, prob.n_o_rows), dtype=torch.float32, device=dev)
@@ -345,7 +351,7 @@ def run_ours(args, rank, world, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "B": w.B, "H": w.H, "D": w.D, "Lq": w.Lq,
+        "config": {"workload": args.workload, "B": prob.B, "H": w.H, "D": w.D, "Lq": w.Lq,
                    "mode": w.mode, "lengths": list(map(str, w.lengths)), "seed": args.seed,
                    "sum_kv_tokens": int(prob.kv_offsets[-1]),
                    "l2": f"inputs larger than L2 (K+V {kv_gb:.2f} GB per step), no flush",
@@ -424,6 +430,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="keep only the first B sequences of the workload (profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -175,7 +175,11 @@ def make_problem(B: int, H: int, D: int, mode: str, kv_lengths, *, Lq: int = 0,
     return Problem(B, H, D, mode, Lq, kv_off, q_off, q, k, v, dout, 1.0 / math.sqrt(D))
 
 
-def make_workload(name: str, seed: int = 0, device="cpu") -> Problem:
+def make_workload(name: str, seed: int = 0, device="cpu", batch: int | None = None) -> Problem:
+    """A named workload; ``batch`` keeps only its first ``batch`` sequences
+    (same length draw), for smaller captures of the same shape mix."""
     w = WORKLOADS[name]
     lengths = draw_lengths(w.lengths, w.B, seed)
-    return make_problem(w.B, w.H, w.D, w.mode, lengths, Lq=w.Lq, seed=seed, device=device)
+    if batch is not None:
+        lengths = lengths[:batch]
+    return make_problem(lengths.size, w.H, w.D, w.mode, lengths, Lq=w.Lq, seed=seed, device=device)
