@@ -156,6 +156,41 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
  */
 int jfa_plan_device_status(jfa_plan_t plan, void* stream, int* raw);
 
+/*
+ * Backward for callers that cannot allocate device memory: code that runs
+ * inside a framework whose caching or pool allocator owns all device memory
+ * (a stray cudaMalloc there fragments or oversubscribes the pool, and
+ * cudaFree synchronises the device), and embedded or serving runtimes that
+ * are handed a fixed budget of pre-allocated buffers and may not grow it.
+ * There is no counterpart of this entry point on the jagged FlashAttention
+ * pages; it computes exactly what jfa_bwd computes (same inputs, outputs,
+ * layouts and tolerances) but needs neither a plan nor a workspace.
+ *
+ * Arguments are those of jfa_plan_create (host offsets, B, H, Lq, D) followed
+ * by those of jfa_bwd without workspace; device_status is an optional device
+ * int the kernels set when a wait runs out (NULL: not reported).
+ *
+ * Scratch: the schedule, the device copy of the offsets and the Delta row
+ * sums live in one file-scope static __device__ array of
+ * JFA_NOALLOC_SCRATCH_BYTES, which every GPU that loads this library holds
+ * until the process exits.  A problem whose scratch (about 4 * H * n_o bytes
+ * of Delta plus 16 bytes per backward tile) does not fit is rejected with
+ * JFA_ERR_WORKSPACE before anything is launched.  The call allocates no
+ * device memory and calls no allocating library routine.
+ *
+ * The first call on a device resolves the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and each call
+ * rewrites what it needs (nothing is assumed to start at zero), so calls
+ * that overlap on the GPU -- different streams, or different host threads
+ * without ordering -- race; issue them on one stream or order them.
+ */
+#define JFA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                    int Lq, int D, const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, float scale, float* dq, void* dk, void* dv,
+                    int* device_status, void* stream);
+
 /* Human-readable text of a status code (static storage). */
 const char* jfa_status_string(int status);
 

@@ -350,3 +350,135 @@ int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward without device allocation (jfa_bwd_noalloc in jfa.h).
+// ---------------------------------------------------------------------------
+namespace {
+
+// The scratch every jfa_bwd_noalloc call uses: a status word, the offsets, the
+// schedule and the Delta row sums.  Host code never hands this symbol to a
+// kernel; it uses the device address cudaGetSymbolAddress returns.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[JFA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch on device `dev` (the current device),
+// resolved on the first call for that device.
+int noalloc_scratch(int dev, uint8_t** out) {
+  if (dev < 0 || dev >= kMaxDevices) return JFA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return JFA_ERR_CUDA;
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = static_cast<uint8_t*>(g_noalloc_addr[dev]);
+  return JFA_OK;
+}
+
+}  // namespace
+
+extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_offsets_host,
+                               int B, int H, int Lq, int D, const void* q, const void* k,
+                               const void* v, const void* out, const void* dout, const float* lse,
+                               float scale, float* dq, void* dk, void* dv, int* device_status,
+                               void* stream) {
+  if (!kv_offsets_host || B < 1 || H < 1 || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+  std::vector<int64_t> qlen, kvlen;
+  int64_t n_kv = 0, n_q = 0;
+  int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
+  if (rc != JFA_OK) return rc;
+  const int64_t n_o = q_offsets_host ? n_q : int64_t(B) * Lq;
+  if (n_o >= (int64_t(1) << 31)) return JFA_ERR_UNSUPPORTED;
+  if ((n_q > 0 && (!q || !dq)) || (n_kv > 0 && (!k || !v || !dk || !dv)) ||
+      (n_o > 0 && (!out || !dout || !lse)))
+    return JFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(device_status) & 3u))
+    return JFA_ERR_ALIGNMENT;
+
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  if (major != 10 || minor != 3) return JFA_ERR_UNSUPPORTED;
+
+  const Schedule sched = jfa::build_bwd_schedule(qlen, kvlen, H, sms);
+  // scratch layout: status | kv offsets | q offsets | tiles | cta_ptr | Delta
+  const size_t o_st = 0;
+  const size_t o_kv = 256;
+  const size_t o_q = align_up(o_kv + (B + 1) * 4, 256);
+  const size_t o_t = align_up(o_q + (q_offsets_host ? (B + 1) * 4 : 0), 256);
+  const size_t o_p = align_up(o_t + sched.tiles.size() * 4, 256);
+  const size_t o_d = align_up(o_p + sched.cta_ptr.size() * 4, 256);
+  const size_t need = o_d + static_cast<size_t>(n_o) * H * sizeof(float);
+  if (need > JFA_NOALLOC_SCRATCH_BYTES) return JFA_ERR_WORKSPACE;
+
+  uint8_t* scratch = nullptr;
+  rc = noalloc_scratch(dev, &scratch);
+  if (rc != JFA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // every byte before Delta is rewritten by this call (the status word
+  // starts at 0); Delta is written in full by the pre-pass below
+  std::vector<uint8_t> host(o_d, 0);
+  std::memcpy(&host[o_kv], kv_offsets_host, (B + 1) * 4);
+  if (q_offsets_host) std::memcpy(&host[o_q], q_offsets_host, (B + 1) * 4);
+  if (!sched.tiles.empty()) std::memcpy(&host[o_t], sched.tiles.data(), sched.tiles.size() * 4);
+  std::memcpy(&host[o_p], sched.cta_ptr.data(), sched.cta_ptr.size() * 4);
+  if (cudaMemcpyAsync(scratch, host.data(), o_d, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return JFA_ERR_CUDA;
+
+  const int64_t cols = int64_t(H) * D;
+  if (n_q > 0 &&
+      cudaMemsetAsync(dq, 0, static_cast<size_t>(n_q) * cols * sizeof(float), s) != cudaSuccess)
+    return JFA_ERR_CUDA;
+  for (int b = 0; b < B; ++b) {  // keys without queries: zero gradients
+    if (qlen[b] == 0 && kvlen[b] > 0) {
+      const size_t off = static_cast<size_t>(kv_offsets_host[b]) * cols * 2;
+      const size_t len = static_cast<size_t>(kvlen[b]) * cols * 2;
+      if (cudaMemsetAsync(static_cast<uint8_t*>(dk) + off, 0, len, s) != cudaSuccess ||
+          cudaMemsetAsync(static_cast<uint8_t*>(dv) + off, 0, len, s) != cudaSuccess)
+        return JFA_ERR_CUDA;
+    }
+  }
+  if (sched.P == 0 || n_o == 0) return JFA_OK;
+  float* delta = reinterpret_cast<float*>(scratch + o_d);
+  cudaError_t e = jfa::launch_delta(static_cast<const uint16_t*>(out),
+                                    static_cast<const uint16_t*>(dout), delta, n_o, H, D, s);
+  if (e != cudaSuccess) return JFA_ERR_CUDA;
+  CUtensorMap qm, km, vm, dom;
+  if (make_map(&qm, q, n_q, cols) || make_map(&km, k, n_kv, cols) || make_map(&vm, v, n_kv, cols) ||
+      make_map(&dom, dout, n_o, cols))
+    return JFA_ERR_CUDA;
+  jfa::BwdArgs a;
+  a.pb.kv_off = reinterpret_cast<const int32_t*>(scratch + o_kv);
+  a.pb.q_off = q_offsets_host ? reinterpret_cast<const int32_t*>(scratch + o_q) : nullptr;
+  a.pb.B = B;
+  a.pb.H = H;
+  a.pb.Lq = q_offsets_host ? 0 : Lq;
+  a.pb.D = D;
+  a.pb.n_q = n_q;
+  a.pb.n_o = n_o;
+  a.pb.n_kv = n_kv;
+  a.tiles = reinterpret_cast<const int32_t*>(scratch + o_t);
+  a.cta_ptr = reinterpret_cast<const int32_t*>(scratch + o_p);
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.lse = lse;
+  a.delta = delta;
+  a.dq = dq;
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.status = device_status ? device_status : reinterpret_cast<int*>(scratch + o_st);
+  e = jfa::launch_bwd(a, qm, km, vm, dom, sched.P, s);
+  return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+

@@ -1,0 +1,90 @@
+"""The backward entry point that allocates no device memory.
+
+jfa_bwd_noalloc serves callers that cannot call cudaMalloc -- code inside a
+framework whose pool allocator owns the device memory, or runtimes handed a
+fixed set of pre-allocated buffers -- by keeping its schedule, offsets and
+Delta row sums in a static device array instead of a plan and a workspace.
+This file is collected last so that a run stopping at the first failure has
+already run every other test.  Each case calls the entry point twice in a row
+through the C ABI (the second call reuses the array the first one filled) and
+compares dQ, dK and dV with jfa_bwd's, within the parity tests' relative-L2
+tolerance.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import jagged_attention_gb300 as jfa
+import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+_vp = ctypes.c_void_p
+
+
+def _entry():
+    L = jfa.lib()
+    fn = L.jfa_bwd_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [jfa._i32p, jfa._i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
+    return fn
+
+
+def _call(fn, p, out, lse, status):
+    kv = jfa._offsets(p.kv_offsets)
+    qo = jfa._offsets(p.q_offsets)
+    dq = torch.full(p.q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    dk = torch.full(p.k.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    dv = torch.full(p.v.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc = fn(jfa._i32ptr(kv), jfa._i32ptr(qo), p.B, p.H, p.Lq, p.D, p.q.data_ptr(), p.k.data_ptr(),
+            p.v.data_ptr(), out.data_ptr(), p.dout.data_ptr(), lse.data_ptr(), p.scale,
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), status.data_ptr(),
+            torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, jfa.STATUS_NAMES.get(rc, rc)
+    return dq, dk, dv
+
+
+CASES = {
+    "tiny_broadcast": lambda: workloads.make_workload("tiny_broadcast", seed=0),
+    "jagged_self": lambda: workloads.make_workload("jagged_self", seed=1),
+    "broadcast_edges": lambda: workloads.make_problem(6, 3, 128, "broadcast",
+                                                      [5, 0, 128, 129, 1000, 300], Lq=200, seed=4),
+    "cross_queryless": lambda: workloads.make_problem(5, 2, 64, "self", [100, 300, 7, 0, 129],
+                                                      q_lengths=[130, 2, 0, 50, 256], seed=5),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_noalloc_matches_jfa_bwd_twice_in_a_row(name):
+    jfa.build()
+    fn = _entry()
+    p = parity.to_cuda(CASES[name]())
+    plan = parity.make_plan(p)
+    out, lse, _ = parity.gpu_fwd(p, plan)
+    ref = parity.gpu_bwd(p, out, lse, plan)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        got = _call(fn, p, out, lse, status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        for g, r in zip(got, ref):
+            assert torch.isfinite(g.float()).all()
+            assert parity.rel_l2(g, r) <= parity.TOL_GRAD
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    jfa.build()
+    fn = _entry()
+    # 2^20 broadcast rows x 16 heads of Delta (64 MiB) cannot fit the 32 MiB
+    # array: the call must refuse before launching anything (tiny real buffers
+    # stand in for the tensors it never touches)
+    t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    f = torch.zeros(16, dtype=torch.float32, device="cuda")
+    kv = jfa._offsets([0, 1])
+    rc = fn(jfa._i32ptr(kv), None, 1, 16, 1 << 20, 64, t.data_ptr(), t.data_ptr(), t.data_ptr(),
+            t.data_ptr(), t.data_ptr(), f.data_ptr(), 0.125, f.data_ptr(), t.data_ptr(),
+            t.data_ptr(), None, torch.cuda.current_stream().cuda_stream)
+    assert rc == 5  # JFA_ERR_WORKSPACE
