@@ -10,7 +10,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/jfa.h"
+#include "jfa.h"
 #include "kernels.h"
 #include "plan.h"
 

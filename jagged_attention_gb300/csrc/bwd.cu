@@ -75,8 +75,7 @@ struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = 128 * 128;       // [128 rows x 64 bf16]
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffKV = 0;                    // two K/V buffers; see bwd_producer
   static constexpr int kOffQ = 2 * kTileBytes;        // 2 stages
   static constexpr int kOffDO = 4 * kTileBytes;       // 2 stages
   static constexpr int kOffDS = 6 * kTileBytes;       // dS^T [128 keys x 128 queries] bf16
@@ -88,18 +87,20 @@ struct BwdCfg {
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 448;
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
+  static constexpr int kDrainWarp0 = 10;  // warps 10-13
 };
 
 struct BwdBars {
-  uint64_t kv_full, kv_empty;
+  uint64_t kv_full[2], kv_empty[2];
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t dv_done, ds_empty;
   uint64_t dq_full, dq_empty;
   uint64_t dkv_full, dkv_empty;
+  uint64_t lse_ready[2], lse_done[2];  // per softmax group: LSE / Delta staging
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -133,23 +134,33 @@ __device__ void bwd_producer(const BwdArgs& a, const CUtensorMap* q_map, const C
   tma_prefetch_desc(k_map);
   tma_prefetch_desc(v_map);
   tma_prefetch_desc(do_map);
-  uint32_t ntile = 0, nq = 0;  // K/V and Q/dO stage loads issued
+  // Two K/V buffers swap roles every tile: tile u keeps K in buffer u % 2
+  // and V in the other.  V is last read by the tile's last dP product, long
+  // before K (last read by the last dQ product), so the next tile's K goes
+  // into the buffer V frees and is resident by the time that tile starts; the
+  // next V follows into the old K buffer, in time for the first dP (which
+  // comes after the first S and P).  Each buffer is filled once per tile.
+  uint32_t nq = 0, nf[2] = {0, 0};  // Q/dO stage loads, fills per K/V buffer
   bool ok = true;
-  for (int i = t_begin; i < t_end && ok; ++i) {
+  uint32_t u = 0;
+  for (int i = t_begin; i < t_end && ok; ++i, ++u) {
     const BTile t = load_btile(a.tiles, i);
     const int x0 = t.h * D;
     const int k_row0 = a.pb.kv_off[t.b] + t.n * 128;
     const int q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
     const int o_base = a.pb.q_off ? a.pb.q_off[t.b] : t.b * a.pb.Lq;
-    ok = mbar_wait(smem_u32(&bars.kv_empty), (ntile & 1) ^ 1, ab);
-    if (!ok) break;
-    mbar_arrive_expect_tx(smem_u32(&bars.kv_full), 2 * C::kTileBytes);
+    const uint32_t kb = u & 1, vb = kb ^ 1;
+    auto load_kv = [&](uint32_t buf, const CUtensorMap* map) -> bool {
+      if (!mbar_wait(smem_u32(&bars.kv_empty[buf]), (u & 1) ^ 1, ab)) return false;
+      mbar_arrive_expect_tx(smem_u32(&bars.kv_full[buf]), C::kTileBytes);
 #pragma unroll
-    for (int c = 0; c < C::kChunks; ++c) {
-      tma_load_2d(sbase + C::kOffK + c * C::kChunkBytes, k_map, smem_u32(&bars.kv_full), x0 + c * 64, k_row0);
-      tma_load_2d(sbase + C::kOffV + c * C::kChunkBytes, v_map, smem_u32(&bars.kv_full), x0 + c * 64, k_row0);
-    }
-    ++ntile;
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_2d(sbase + C::kOffKV + buf * C::kTileBytes + c * C::kChunkBytes, map,
+                    smem_u32(&bars.kv_full[buf]), x0 + c * 64, k_row0);
+      ++nf[buf];
+      return true;
+    };
+    ok = load_kv(kb, k_map);
     for (int m = 0; m < t.qblocks && ok; ++m) {
       const uint32_t qs = nq & 1, ph = (nq >> 1) & 1;
       ok = mbar_wait(smem_u32(&bars.q_empty[qs]), ph ^ 1, ab);
@@ -163,10 +174,12 @@ __device__ void bwd_producer(const BwdArgs& a, const CUtensorMap* q_map, const C
                     smem_u32(&bars.q_full[qs]), x0 + c * 64, o_base + m * 128);
       }
       ++nq;
+      if (m == 0) ok = load_kv(vb, v_map);
     }
   }
   // let every issued copy land before the CTA may exit
-  if (ntile > 0) drain_wait_b(smem_u32(&bars.kv_full), (ntile - 1) & 1);
+  for (int b = 0; b < 2; ++b)
+    if (nf[b] > 0) drain_wait_b(smem_u32(&bars.kv_full[b]), (nf[b] - 1) & 1);
   for (uint32_t qs = 0; qs < 2 && qs < nq; ++qs) {
     const uint32_t last = nq - 1 - ((nq - 1 - qs) & 1);
     drain_wait_b(smem_u32(&bars.q_full[qs]), (last >> 1) & 1);
@@ -181,17 +194,20 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
   constexpr uint32_t id_sdp = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   constexpr uint32_t id_kmaj = idesc_bf16_f32(128, D, false, true);    // dV (A in TMEM), dK
   constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);       // dQ: A = dS (M-major)
-  const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sDS = sbase + C::kOffDS;
+  const uint32_t sDS = sbase + C::kOffDS;
   uint32_t gm = 0, tt = 0;
   bool ok = true;
   for (int i = t_begin; i < t_end && ok; ++i) {
     const BTile t = load_btile(a.tiles, i);
+    const uint32_t kb = tt & 1, vb = kb ^ 1;  // K and V buffers of this tile
+    const uint32_t sK = sbase + C::kOffKV + kb * C::kTileBytes;
+    const uint32_t sV = sbase + C::kOffKV + vb * C::kTileBytes;
     for (int m = 0; m < t.qblocks && ok; ++m, ++gm) {
       const uint32_t qs = gm & 1;
       const uint32_t sQ = sbase + C::kOffQ + qs * C::kTileBytes;
       const uint32_t sDO = sbase + C::kOffDO + qs * C::kTileBytes;
       ok = mbar_wait(smem_u32(&bars.q_full[qs]), (gm >> 1) & 1, ab);
-      if (ok && m == 0) ok = mbar_wait(smem_u32(&bars.kv_full), tt & 1, ab);
+      if (ok && m == 0) ok = mbar_wait(smem_u32(&bars.kv_full[kb]), tt & 1, ab);
       // S^T region is free once the previous step's dV (which read P^T there) completed
       if (ok) ok = mbar_wait(smem_u32(&bars.dv_done), (gm & 1) ^ 1, ab);
       if (!ok) break;
@@ -205,6 +221,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
       mma_commit(smem_u32(&bars.s_full));
       // dP^T region is free once WG1 has the previous dQ in registers
       ok = mbar_wait(smem_u32(&bars.dq_empty), (gm & 1) ^ 1, ab);
+      if (ok && m == 0) ok = mbar_wait(smem_u32(&bars.kv_full[vb]), tt & 1, ab);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -214,13 +231,15 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
                     smem_desc_sw128(sDO + koff, 16, 1024), id_sdp, kk > 0 ? 1u : 0u);
       }
       mma_commit(smem_u32(&bars.dp_full));
+      if (m == t.qblocks - 1) mma_commit(smem_u32(&bars.kv_empty[vb]));  // V read for the last time
       if (m == 0) ok = mbar_wait(smem_u32(&bars.dkv_empty), (tt & 1) ^ 1, ab);
       if (ok) ok = mbar_wait(smem_u32(&bars.p_full), gm & 1, ab);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_m, K = 128 queries
-        mma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
+      for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_m, K = 128 queries; P^T of query
+                                       // half g sits at S columns [64g, 64g + 32)
+        mma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                     smem_desc_sw128(sDO + kk * 2048, C::kChunkBytes, 1024), id_kmaj,
                     (m > 0 || kk > 0) ? 1u : 0u);
       mma_commit(smem_u32(&bars.dv_done));
@@ -243,7 +262,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
       mma_commit(smem_u32(&bars.q_empty[qs]));
       if (m == t.qblocks - 1) {
         mma_commit(smem_u32(&bars.dkv_full));
-        mma_commit(smem_u32(&bars.kv_empty));
+        mma_commit(smem_u32(&bars.kv_empty[kb]));  // K read for the last time
       }
     }
     ++tt;
@@ -253,16 +272,22 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
 }
 
 // ---------------------------------------------------------------------------
-// WG0: P^T and dS^T, one thread per key row (TMEM lane)
+// Softmax groups: P^T and dS^T.  Two warpgroups share every key row (TMEM
+// lane): group g (warps 4g .. 4g+3) owns query columns [64g, 64g + 64).  The
+// backward needs no row reduction (LSE and Delta are given), so the halves
+// are independent; splitting them puts two warps on every SM sub-partition,
+// which keeps the exp2 unit and the TMEM traffic busy.
 template <int D>
-__device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uint32_t tmem, BwdBars& bars,
-                            const Abort& ab, int t_begin, int t_end) {
+__device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uint32_t tmem,
+                            BwdBars& bars, const Abort& ab, int t_begin, int t_end, int g) {
   using C = BwdCfg<D>;
-  const int r = threadIdx.x;  // 0..127
-  const int warp = r >> 5;
-  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = (warp & 3) * 32 + lane;  // key row of the tile = TMEM lane
+  const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const int c0 = 64 * g;                 // first query column of this group
   float* lse2 = reinterpret_cast<float*>(smem + C::kOffLse);  // 128 LSE*log2(e), then 128 Delta
   float* dlt = lse2 + 128;
+  const uint32_t lse_ready = smem_u32(&bars.lse_ready[g]), lse_done = smem_u32(&bars.lse_done[g]);
   uint32_t gm = 0;
   for (int i = t_begin; i < t_end; ++i) {
     const BTile t = load_btile(a.tiles, i);
@@ -271,42 +296,38 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
     const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + 1] - a.pb.q_off[t.b]) : a.pb.Lq;
     const int64_t o_base = a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq;
     for (int m = 0; m < t.qblocks; ++m, ++gm) {
-      // per-query LSE (log2 units) and Delta of this block, masked past the sequence
-      named_bar_sync(1, 128);  // everyone is done with the previous block's values
-      {
-        const bool q_ok = int64_t(m) * 128 + r < qlen;
-        const int64_t idx = int64_t(t.h) * a.pb.n_o + o_base + m * 128 + r;
-        lse2[r] = q_ok ? a.lse[idx] * 1.4426950408889634f : INFINITY;
-        dlt[r] = q_ok ? a.delta[idx] : 0.0f;
+      // this group's 64 LSE (log2 units) and Delta values, masked past the
+      // sequence; mbarriers (bounded waits) rather than hardware barriers, so a
+      // timed-out warp can never strand the others
+      if (!warp_wait_b(lse_done, (gm & 1) ^ 1, ab)) return;  // previous block's values read
+      if (r < 64) {
+        const int64_t q = int64_t(m) * 128 + c0 + r;
+        const bool q_ok = q < qlen;
+        const int64_t idx = int64_t(t.h) * a.pb.n_o + o_base + q;
+        lse2[c0 + r] = q_ok ? a.lse[idx] * 1.4426950408889634f : INFINITY;
+        dlt[c0 + r] = q_ok ? a.delta[idx] : 0.0f;
       }
-      named_bar_sync(1, 128);
+      mbar_arrive(lse_ready);
+      if (!warp_wait_b(lse_ready, gm & 1, ab)) return;
 
       if (!warp_wait_b(smem_u32(&bars.s_full), gm & 1, ab)) return;
       tc_fence_after();
-      uint32_t p[64];  // P^T row, bf16 pairs
+      uint32_t p[32];  // this row's 64 P^T values, bf16 pairs
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld_x32(tl + C::kColS + c * 32, v);
+        tmem_ld_x32(tl + C::kColS + c0 + c * 32, v);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int j = c * 32 + 2 * e;
+          const int j = c0 + c * 32 + 2 * e;
           float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, -lse2[j]));
           float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, -lse2[j + 1]));
           if (!kv_ok) p0 = p1 = 0.0f;
           p[c * 16 + e] = pack_bf16x2(p0, p1);
         }
       }
-      {
-        uint32_t lo[32], hi[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          lo[e] = p[e];
-          hi[e] = p[32 + e];
-        }
-        tmem_st_x32(tl + C::kColS, lo);
-        tmem_st_x32(tl + C::kColS + 32, hi);
-      }
+      // P^T back into TMEM over this group's own (already read) S columns
+      tmem_st_x32(tl + C::kColS + c0, p);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full));
@@ -315,43 +336,86 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
       // the dS^T buffer is free once the previous step's dK and dQ products completed
       if (!warp_wait_b(smem_u32(&bars.ds_empty), (gm & 1) ^ 1, ab)) return;
       tc_fence_after();
-      const uint32_t sDS = sbase + C::kOffDS;
+      const uint32_t sDS = sbase + C::kOffDS + g * C::kChunkBytes;  // 128-byte chunk g of each row
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld_x32(tl + C::kColDP + c * 32, v);
+        tmem_ld_x32(tl + C::kColDP + c0 + c * 32, v);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int j = c * 32 + 2 * e;
+          const int j = c0 + c * 32 + 2 * e;
           const uint32_t pp = p[c * 16 + e];
           const float d0 = __uint_as_float(pp << 16) * (__uint_as_float(v[2 * e]) - dlt[j]);
           const float d1 = __uint_as_float(pp & 0xffff0000u) * (__uint_as_float(v[2 * e + 1]) - dlt[j + 1]);
           w[e] = pack_bf16x2(d0, d1);
         }
-        // query columns 32c..32c+31 = 128-byte chunk c/2, 16-byte units (c%2)*4 .. +3
-        const uint32_t base = sDS + (c >> 1) * C::kChunkBytes;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(base + sw128_offset(r, (c & 1) * 4 + q4), w[4 * q4], w[4 * q4 + 1],
-                       w[4 * q4 + 2], w[4 * q4 + 3]);
+          st_shared_v4(sDS + sw128_offset(r, c * 4 + q4), w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2],
+                       w[4 * q4 + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.ds_full));
+      mbar_arrive(lse_done);  // this block's LSE / Delta no longer read by this thread
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// WG1: dQ drain (thread = query row) and the dK / dV epilogue (thread = key row)
+// Drain group (warps 10-13): dQ_m leaves TMEM (thread = query row) in two
+// passes of 64 columns, the TMEM columns are released as soon as the slice is
+// in registers, and the fp32 vector reduce-adds into dq follow (the cross-batch
+// reduction of the broadcast mode happens here, in the memory system).  At the
+// end of a tile the group writes dV and scale * dK (thread = key row) before
+// the tile's last dQ reductions, so the next tile's products do not wait for
+// them.
+template <int D>
+__device__ __forceinline__ void dkv_epilogue(const BwdArgs& a, uint32_t tl, const BTile& t, int r) {
+  using C = BwdCfg<D>;
+  const int H = a.pb.H;
+  const int64_t klen = a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b];
+  const bool kv_ok = int64_t(t.n) * 128 + r < klen;
+  const int64_t krow = int64_t(a.pb.kv_off[t.b]) + t.n * 128 + r;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+    const float mul = which == 0 ? 1.0f : a.scale;
+    uint16_t* dst_row = (which == 0 ? a.dv : a.dk) + (krow * H + t.h) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t w[32];
+      tmem_ld_x32(tl + col + c * 32, w);
+      if (kv_ok) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(w[2 * e]) * mul, __uint_as_float(w[2 * e + 1]) * mul);
+        uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void dq_reduce(float* row, const uint32_t (&v)[64], float scale) {
+  float4* dst = reinterpret_cast<float4*>(row);
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]) * scale, __uint_as_float(v[4 * e + 1]) * scale,
+                                   __uint_as_float(v[4 * e + 2]) * scale, __uint_as_float(v[4 * e + 3]) * scale));
+}
+
 template <int D>
 __device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const Abort& ab,
                           int t_begin, int t_end) {
   using C = BwdCfg<D>;
-  const int r = threadIdx.x - 128;  // 0..127
-  const int warp = r >> 5;          // TMEM lane quarter: warps 4-7 -> 0-3
-  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = (warp & 3) * 32 + lane;  // TMEM lane of this thread
+  const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int H = a.pb.H;
   uint32_t gm = 0, tt = 0;
   for (int i = t_begin; i < t_end; ++i) {
@@ -359,57 +423,46 @@ __device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const 
     const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + 1] - a.pb.q_off[t.b]) : a.pb.Lq;
     const int64_t q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
     for (int m = 0; m < t.qblocks; ++m, ++gm) {
+      if (m == t.qblocks - 1) {
+        if (!warp_wait_b(smem_u32(&bars.dkv_full), tt & 1, ab)) return;
+        tc_fence_after();
+        dkv_epilogue<D>(a, tl, t, r);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dkv_empty));
+        ++tt;
+      }
       if (!warp_wait_b(smem_u32(&bars.dq_full), gm & 1, ab)) return;
       tc_fence_after();
-      uint32_t v[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      const bool q_ok = int64_t(m) * 128 + r < qlen;
+      float* row = a.dq + ((q_base + int64_t(m) * 128 + r) * H + t.h) * D;
+      uint32_t v[64];
+      {
         uint32_t w[32];
-        tmem_ld_x32(tl + C::kColDP + c * 32, w);
+        tmem_ld_x32(tl + C::kColDP, w);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[c * 32 + e] = w[e];
+        for (int e = 0; e < 32; ++e) v[e] = w[e];
+        tmem_ld_x32(tl + C::kColDP + 32, w);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[32 + e] = w[e];
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.dq_empty));  // TMEM released before the global reductions
-      if (int64_t(m) * 128 + r < qlen) {
-        float4* dst = reinterpret_cast<float4*>(a.dq + ((q_base + m * 128 + r) * H + t.h) * D);
+      if constexpr (D == 128) {
+        if (q_ok) dq_reduce<D>(row, v, a.scale);
+        uint32_t w[32];
+        tmem_ld_x32(tl + C::kColDP + 64, w);
 #pragma unroll
-        for (int e = 0; e < D / 4; ++e)
-          atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]) * a.scale,
-                                         __uint_as_float(v[4 * e + 1]) * a.scale,
-                                         __uint_as_float(v[4 * e + 2]) * a.scale,
-                                         __uint_as_float(v[4 * e + 3]) * a.scale));
+        for (int e = 0; e < 32; ++e) v[e] = w[e];
+        tmem_ld_x32(tl + C::kColDP + 96, w);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[32 + e] = w[e];
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_empty));  // TMEM released before the last reductions
+        if (q_ok) dq_reduce<D>(row + 64, v, a.scale);
+      } else {
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_empty));
+        if (q_ok) dq_reduce<D>(row, v, a.scale);
       }
     }
-    // tile done: dV and scale * dK rows in bf16
-    if (!warp_wait_b(smem_u32(&bars.dkv_full), tt & 1, ab)) return;
-    tc_fence_after();
-    const int64_t klen = a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b];
-    const bool kv_ok = int64_t(t.n) * 128 + r < klen;
-    const int64_t krow = int64_t(a.pb.kv_off[t.b]) + t.n * 128 + r;
-#pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
-      const float mul = which == 0 ? 1.0f : a.scale;
-      uint16_t* dst_row = (which == 0 ? a.dv : a.dk) + (krow * H + t.h) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t w[32];
-        tmem_ld_x32(tl + col + c * 32, w);
-        if (kv_ok) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(w[2 * e]) * mul, __uint_as_float(w[2 * e + 1]) * mul);
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        }
-      }
-    }
-    tc_fence_before();
-    mbar_arrive(smem_u32(&bars.dkv_empty));
-    ++tt;
   }
 }
 
@@ -427,22 +480,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t_begin = a.cta_ptr[blockIdx.x], t_end = a.cta_ptr[blockIdx.x + 1];
   if (tid == 0) {
-    mbar_init(smem_u32(&bars.kv_full), 1);
-    mbar_init(smem_u32(&bars.kv_empty), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars.kv_full[b]), 1);
+      mbar_init(smem_u32(&bars.kv_empty[b]), 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.q_full[s]), 1);
       mbar_init(smem_u32(&bars.q_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars.s_full), 1);
     mbar_init(smem_u32(&bars.dp_full), 1);
-    mbar_init(smem_u32(&bars.p_full), 128);
-    mbar_init(smem_u32(&bars.ds_full), 128);
+    mbar_init(smem_u32(&bars.p_full), 256);
+    mbar_init(smem_u32(&bars.ds_full), 256);
     mbar_init(smem_u32(&bars.dv_done), 1);
     mbar_init(smem_u32(&bars.ds_empty), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_empty), 128);
     mbar_init(smem_u32(&bars.dkv_full), 1);
     mbar_init(smem_u32(&bars.dkv_empty), 128);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(smem_u32(&bars.lse_ready[g]), 128);
+      mbar_init(smem_u32(&bars.lse_done[g]), 128);
+    }
     mbar_init(smem_u32(&bars.drain), 1);
     bars.abort_flag = 0;
     fence_mbar_init();
@@ -456,9 +515,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   const Abort ab{&bars.abort_flag, a.status};
-  if (warp < 4) {
-    bwd_softmax<D>(a, smem, sbase, tmem, bars, ab, t_begin, t_end);
-  } else if (warp < 8) {
+  if (warp < 8) {
+    bwd_softmax<D>(a, smem, sbase, tmem, bars, ab, t_begin, t_end, warp >> 2);
+  } else if (warp >= C::kDrainWarp0) {
     bwd_drain<D>(a, tmem, bars, ab, t_begin, t_end);
   } else if (warp == C::kProducerWarp) {
     if (lane == 0) bwd_producer<D>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, t_begin, t_end);
