@@ -88,6 +88,25 @@ typedef struct jfa_plan* jfa_plan_t;
 int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                     int Lq, int D, int num_ctas, void* stream, jfa_plan_t* out);
 
+/*
+ * Plan flags.
+ * JFA_PLAN_PACK_SHORT: in self mode with one offsets array shared by queries
+ * and keys (q_offsets equal to kv_offsets element by element), runs of
+ * consecutive short sequences whose lengths add up to at most 128 rows (with
+ * at least two non-empty ones) share one 128-row tile, masked block-diagonally
+ * so every row still sees only its own sequence.  This is the block-diagonal
+ * case of the TLX Block Attention page ("One Constraint, Five Eliminations":
+ * each query tile meets exactly one key tile), which the plain schedule runs
+ * at half occupancy when segments are shorter than a tile.  Such a tile is
+ * recorded as {b0, h, -nseq, 1}.  Ignored in broadcast mode or when the
+ * offsets differ.
+ */
+#define JFA_PLAN_PACK_SHORT 1u
+
+/* jfa_plan_create with flags (0 = the schedule described above). */
+int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                       int Lq, int D, int num_ctas, unsigned flags, void* stream, jfa_plan_t* out);
+
 /* Release a plan (synchronises the device first so in-flight work finishes). */
 int jfa_plan_destroy(jfa_plan_t plan);
 
@@ -102,14 +121,14 @@ int jfa_plan_tiles(jfa_plan_t plan, int dir, int32_t* tiles_host, int32_t* cta_p
                    int* P);
 
 /*
- * Host-only schedule builder (no GPU needed): the same lists a plan holds,
- * from host lengths.  q_lengths == NULL means broadcast with Lq rows.  Call
- * once with tiles_out == NULL to learn *T and *P, then with buffers of 4*T
- * and P+1 int32.
+ * Host-only schedule builder (no GPU needed): the same lists a plan created
+ * with the same flags holds.  q_offsets_host == NULL means broadcast with Lq
+ * rows.  Call once with tiles_out == NULL to learn *T and *P, then with
+ * buffers of 4*T and P+1 int32.
  */
 int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
-                    int Lq, int num_ctas, int dir, int32_t* tiles_out, int32_t* cta_ptr_out, int* T,
-                    int* P);
+                    int Lq, int num_ctas, int dir, unsigned flags, int32_t* tiles_out,
+                    int32_t* cta_ptr_out, int* T, int* P);
 
 /*
  * Forward: out = softmax(scale Q K^T) V per sequence and head, lse as above.
@@ -138,8 +157,9 @@ int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const 
 /*
  * The two stages jfa_bwd runs, for callers that schedule them separately
  * (same arguments and rules as jfa_bwd).
- * jfa_bwd_preprocess: Delta (into workspace) from out and dout, clears dq,
- *   and zeroes dk / dv rows of sequences that have keys but no queries.
+ * jfa_bwd_preprocess: Delta (into workspace) from out and dout, clears dq
+ *   (unless every sequence sits in a packed tile, whose dQ rows are stored
+ *   outright), and zeroes dk / dv rows of sequences with keys but no queries.
  * jfa_bwd_main: the key/value-stationary pass; needs the workspace written by
  *   jfa_bwd_preprocess (stream order) and the cleared dq.
  */

@@ -28,6 +28,7 @@ STATUS_NAMES = {
     4: "JFA_ERR_ALIGNMENT", 5: "JFA_ERR_WORKSPACE", 6: "JFA_ERR_CUDA", 7: "JFA_ERR_DEVICE_TIMEOUT",
 }
 BLOCK_M = BLOCK_N = 128
+PLAN_PACK_SHORT = 1  # JFA_PLAN_PACK_SHORT
 
 
 class JfaError(RuntimeError):
@@ -62,7 +63,11 @@ def lib() -> ctypes.CDLL:
             L.jfa_plan_destroy.argtypes = [_vp]
             L.jfa_plan_tiles.argtypes = [_vp, ctypes.c_int, _i32p, _i32p, _ip, _ip]
             L.jfa_build_tiles.argtypes = [_i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                          ctypes.c_int, ctypes.c_int, _i32p, _i32p, _ip, _ip]
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_uint, _i32p, _i32p,
+                                          _ip, _ip]
+            L.jfa_plan_create_ex.argtypes = [_i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_uint, _vp,
+                                             ctypes.POINTER(_vp)]
             L.jfa_fwd.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp]
             L.jfa_bwd_workspace_bytes.argtypes = [_vp]
             L.jfa_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -74,7 +79,7 @@ def lib() -> ctypes.CDLL:
             L.jfa_plan_device_status.argtypes = [_vp, _vp, _ip]
             L.jfa_status_string.argtypes = [ctypes.c_int]
             L.jfa_status_string.restype = ctypes.c_char_p
-            for name in ("jfa_plan_create", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
+            for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
                          "jfa_fwd", "jfa_bwd", "jfa_bwd_preprocess", "jfa_bwd_main",
                          "jfa_plan_device_status"):
                 getattr(L, name).restype = ctypes.c_int
@@ -107,18 +112,19 @@ def _stream(stream) -> int | None:
     return int(stream)
 
 
-def build_tiles(kv_offsets, q_offsets=None, *, H: int, Lq: int = 0, num_ctas: int, direction: int):
+def build_tiles(kv_offsets, q_offsets=None, *, H: int, Lq: int = 0, num_ctas: int, direction: int,
+                flags: int = 0):
     """Host-only schedule (no GPU): tiles int32 [T, 4] and cta_ptr int32 [P + 1]."""
     kv = _offsets(kv_offsets)
     qo = _offsets(q_offsets)
     B = kv.size - 1
     T, P = ctypes.c_int(), ctypes.c_int()
     L = lib()
-    _check(L.jfa_build_tiles(_i32ptr(kv), _i32ptr(qo), B, H, Lq, num_ctas, direction, None, None,
-                             ctypes.byref(T), ctypes.byref(P)), "jfa_build_tiles")
+    _check(L.jfa_build_tiles(_i32ptr(kv), _i32ptr(qo), B, H, Lq, num_ctas, direction, flags, None,
+                             None, ctypes.byref(T), ctypes.byref(P)), "jfa_build_tiles")
     tiles = np.zeros((T.value, 4), dtype=np.int32)
     ptr = np.zeros(P.value + 1, dtype=np.int32)
-    _check(L.jfa_build_tiles(_i32ptr(kv), _i32ptr(qo), B, H, Lq, num_ctas, direction,
+    _check(L.jfa_build_tiles(_i32ptr(kv), _i32ptr(qo), B, H, Lq, num_ctas, direction, flags,
                              tiles.ctypes.data_as(_i32p), ptr.ctypes.data_as(_i32p),
                              ctypes.byref(T), ctypes.byref(P)), "jfa_build_tiles")
     return tiles, ptr
@@ -128,7 +134,7 @@ class Plan:
     """A jfa_plan_t: offsets and tile schedules resident on the current device."""
 
     def __init__(self, kv_offsets, q_offsets=None, *, H: int, D: int, Lq: int = 0,
-                 num_ctas: int = 0, stream=None):
+                 num_ctas: int = 0, flags: int = 0, stream=None):
         self.kv_offsets = _offsets(kv_offsets)
         self.q_offsets = _offsets(q_offsets)
         self.B = self.kv_offsets.size - 1
@@ -139,9 +145,11 @@ class Plan:
         self.n_q = self.Lq if self.broadcast else int(self.q_offsets[-1])
         self.n_o = self.B * self.Lq if self.broadcast else self.n_q
         h = _vp()
-        _check(lib().jfa_plan_create(_i32ptr(self.kv_offsets), _i32ptr(self.q_offsets), self.B, H,
-                                     self.Lq, D, num_ctas, _stream(stream), ctypes.byref(h)),
-               "jfa_plan_create")
+        self.flags = flags
+        _check(lib().jfa_plan_create_ex(_i32ptr(self.kv_offsets), _i32ptr(self.q_offsets), self.B,
+                                        H, self.Lq, D, num_ctas, flags, _stream(stream),
+                                        ctypes.byref(h)),
+               "jfa_plan_create_ex")
         self._h = h
 
     @property

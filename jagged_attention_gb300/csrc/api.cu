@@ -89,6 +89,12 @@ int lengths_of(const int32_t* kv_off, const int32_t* q_off, int B, int Lq,
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Packing needs self mode with one offsets array for queries and keys.
+bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B) {
+  if (!(flags & JFA_PLAN_PACK_SHORT) || !q_off) return false;
+  return std::memcmp(kv_off, q_off, (B + 1) * sizeof(int32_t)) == 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -108,16 +114,19 @@ const char* jfa_status_string(int s) {
 }
 
 int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
-                    int Lq, int num_ctas, int dir, int32_t* tiles_out, int32_t* cta_ptr_out, int* T,
-                    int* P) {
+                    int Lq, int num_ctas, int dir, unsigned flags, int32_t* tiles_out,
+                    int32_t* cta_ptr_out, int* T, int* P) {
   if (!kv_offsets_host || B < 1 || H < 1 || num_ctas < 1 || (dir != 0 && dir != 1) || !T || !P)
     return JFA_ERR_INVALID_ARG;
   std::vector<int64_t> qlen, kvlen;
   int64_t n_kv = 0, n_q = 0;
   int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
   if (rc != JFA_OK) return rc;
-  const Schedule s = dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas)
-                              : jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas);
+  std::vector<int> pack;
+  const bool packing = use_packing(flags, kv_offsets_host, q_offsets_host, B);
+  if (packing) pack = jfa::short_packs(kvlen);
+  const Schedule s = dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr)
+                              : jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr);
   *T = s.T;
   *P = s.P;
   if (tiles_out) std::memcpy(tiles_out, s.tiles.data(), s.tiles.size() * sizeof(int32_t));
@@ -127,6 +136,11 @@ int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
 
 int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                     int Lq, int D, int num_ctas, void* stream, jfa_plan_t* out) {
+  return jfa_plan_create_ex(kv_offsets_host, q_offsets_host, B, H, Lq, D, num_ctas, 0u, stream, out);
+}
+
+int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                       int Lq, int D, int num_ctas, unsigned flags, void* stream, jfa_plan_t* out) {
   if (!out || !kv_offsets_host || B < 1 || H < 1 || num_ctas < 0) return JFA_ERR_INVALID_ARG;
   *out = nullptr;
   if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
@@ -157,8 +171,16 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
   p->n_q = n_q;
   p->n_o = n_o;
   p->n_kv = n_kv;
-  p->fwd = jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas);
-  p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas);
+  std::vector<int> pack;
+  p->packed = use_packing(flags, kv_offsets_host, q_offsets_host, B);
+  if (p->packed) {
+    pack = jfa::short_packs(kvlen);
+    p->all_packed = true;
+    for (int b = 0; b < B; ++b)
+      if (kvlen[b] > 0 && pack[b] == 1) p->all_packed = false;
+  }
+  p->fwd = jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr);
+  p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr);
   for (int b = 0; b < B; ++b) {
     if (qlen[b] == 0 && kvlen[b] > 0) {
       const int64_t s = kv_offsets_host[b], e = kv_offsets_host[b + 1];
@@ -264,6 +286,7 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.status = plan->d_status;
+  a.packed = plan->packed;
   cudaError_t e = jfa::launch_fwd(a, qm, km, vm, plan->fwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -286,8 +309,9 @@ int jfa_bwd_preprocess(jfa_plan_t plan, const void* out, const void* dout, float
     return JFA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t cols = int64_t(plan->H) * plan->D;
-  // dQ is reduce-added by the key/value tiles: start from zero
-  if (plan->n_q > 0 &&
+  // dQ is reduce-added by the key/value tiles: start from zero (packed tiles
+  // store their rows, so a fully packed plan needs no clearing)
+  if (plan->n_q > 0 && !plan->all_packed &&
       cudaMemsetAsync(dq, 0, static_cast<size_t>(plan->n_q) * cols * sizeof(float), s) != cudaSuccess)
     return JFA_ERR_CUDA;
   // keys of sequences without queries get no backward tile: their gradients are zero
@@ -335,6 +359,7 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
   a.status = plan->d_status;
+  a.packed = plan->packed;
   cudaError_t e = jfa::launch_bwd(a, qm, km, vm, dom, plan->bwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -478,6 +503,7 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
   a.status = device_status ? device_status : reinterpret_cast<int*>(scratch + o_st);
+  a.packed = false;
   e = jfa::launch_bwd(a, qm, km, vm, dom, sched.P, s);
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }

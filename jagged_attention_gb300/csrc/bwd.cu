@@ -125,7 +125,7 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kPack>
 __device__ void bwd_producer(const BwdArgs& a, const CUtensorMap* q_map, const CUtensorMap* k_map,
                              const CUtensorMap* v_map, const CUtensorMap* do_map, uint32_t sbase,
                              BwdBars& bars, const Abort& ab, int t_begin, int t_end) {
@@ -146,7 +146,7 @@ __device__ void bwd_producer(const BwdArgs& a, const CUtensorMap* q_map, const C
   for (int i = t_begin; i < t_end && ok; ++i, ++u) {
     const BTile t = load_btile(a.tiles, i);
     const int x0 = t.h * D;
-    const int k_row0 = a.pb.kv_off[t.b] + t.n * 128;
+    const int k_row0 = a.pb.kv_off[t.b] + (kPack ? max(t.n, 0) : t.n) * 128;  // packed tiles: n < 0
     const int q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
     const int o_base = a.pb.q_off ? a.pb.q_off[t.b] : t.b * a.pb.Lq;
     const uint32_t kb = u & 1, vb = kb ^ 1;
@@ -277,7 +277,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
 // backward needs no row reduction (LSE and Delta are given), so the halves
 // are independent; splitting them puts two warps on every SM sub-partition,
 // which keeps the exp2 unit and the TMEM traffic busy.
-template <int D>
+template <int D, bool kPack>
 __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uint32_t tmem,
                             BwdBars& bars, const Abort& ab, int t_begin, int t_end, int g) {
   using C = BwdCfg<D>;
@@ -291,9 +291,22 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
   uint32_t gm = 0;
   for (int i = t_begin; i < t_end; ++i) {
     const BTile t = load_btile(a.tiles, i);
-    const int64_t klen = a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b];
-    const bool kv_ok = int64_t(t.n) * 128 + r < klen;
-    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + 1] - a.pb.q_off[t.b]) : a.pb.Lq;
+    // packed tile (n = -nseq): key and query rows [off[b], off[b + nseq]) of
+    // nseq short sequences; a key row only meets its own sequence's queries
+    const bool packed = kPack && t.n < 0;
+    const int nb = packed ? 0 : t.n;
+    const int b_end = t.b + (packed ? -t.n : 1);
+    const int64_t klen = a.pb.kv_off[b_end] - a.pb.kv_off[t.b];
+    const bool kv_ok = int64_t(nb) * 128 + r < klen;
+    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[b_end] - a.pb.q_off[t.b]) : a.pb.Lq;
+    int q_lo = 0, q_hi = 128;  // query columns this key row may meet
+    if (packed && kv_ok) {
+      const int base = a.pb.kv_off[t.b], row = base + r;
+      int sq = t.b;
+      while (a.pb.kv_off[sq + 1] <= row) ++sq;
+      q_lo = a.pb.kv_off[sq] - base;
+      q_hi = a.pb.kv_off[sq + 1] - base;
+    }
     const int64_t o_base = a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq;
     for (int m = 0; m < t.qblocks; ++m, ++gm) {
       // this group's 64 LSE (log2 units) and Delta values, masked past the
@@ -313,17 +326,34 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
       if (!warp_wait_b(smem_u32(&bars.s_full), gm & 1, ab)) return;
       tc_fence_after();
       uint32_t p[32];  // this row's 64 P^T values, bf16 pairs
+      if (!packed) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld_x32(tl + C::kColS + c0 + c * 32, v);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld_x32(tl + C::kColS + c0 + c * 32, v);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = c0 + c * 32 + 2 * e;
-          float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, -lse2[j]));
-          float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, -lse2[j + 1]));
-          if (!kv_ok) p0 = p1 = 0.0f;
-          p[c * 16 + e] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 16; ++e) {
+            const int j = c0 + c * 32 + 2 * e;
+            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, -lse2[j]));
+            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, -lse2[j + 1]));
+            if (!kv_ok) p0 = p1 = 0.0f;
+            p[c * 16 + e] = pack_bf16x2(p0, p1);
+          }
+        }
+      } else {  // packed tile: only this key row's own sequence
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld_x32(tl + C::kColS + c0 + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = c0 + c * 32 + 2 * e;
+            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, -lse2[j]));
+            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, -lse2[j + 1]));
+            if (!kv_ok || j < q_lo || j >= q_hi) p0 = 0.0f;
+            if (!kv_ok || j + 1 < q_lo || j + 1 >= q_hi) p1 = 0.0f;
+            p[c * 16 + e] = pack_bf16x2(p0, p1);
+          }
         }
       }
       // P^T back into TMEM over this group's own (already read) S columns
@@ -371,13 +401,15 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
 // end of a tile the group writes dV and scale * dK (thread = key row) before
 // the tile's last dQ reductions, so the next tile's products do not wait for
 // them.
-template <int D>
+template <int D, bool kPack>
 __device__ __forceinline__ void dkv_epilogue(const BwdArgs& a, uint32_t tl, const BTile& t, int r) {
   using C = BwdCfg<D>;
   const int H = a.pb.H;
-  const int64_t klen = a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b];
-  const bool kv_ok = int64_t(t.n) * 128 + r < klen;
-  const int64_t krow = int64_t(a.pb.kv_off[t.b]) + t.n * 128 + r;
+  const bool packed = kPack && t.n < 0;  // packed tile: rows of -n short sequences
+  const int nb = packed ? 0 : t.n;
+  const int64_t klen = a.pb.kv_off[t.b + (packed ? -t.n : 1)] - a.pb.kv_off[t.b];
+  const bool kv_ok = int64_t(nb) * 128 + r < klen;
+  const int64_t krow = int64_t(a.pb.kv_off[t.b]) + nb * 128 + r;
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
     const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
@@ -400,16 +432,20 @@ __device__ __forceinline__ void dkv_epilogue(const BwdArgs& a, uint32_t tl, cons
   }
 }
 
+// 64 dQ columns of one row: reduce-added, or stored when this tile owns the row.
 template <int D>
-__device__ __forceinline__ void dq_reduce(float* row, const uint32_t (&v)[64], float scale) {
+__device__ __forceinline__ void dq_out(float* row, const uint32_t (&v)[64], float scale, bool store) {
   float4* dst = reinterpret_cast<float4*>(row);
 #pragma unroll
-  for (int e = 0; e < 16; ++e)
-    atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]) * scale, __uint_as_float(v[4 * e + 1]) * scale,
-                                   __uint_as_float(v[4 * e + 2]) * scale, __uint_as_float(v[4 * e + 3]) * scale));
+  for (int e = 0; e < 16; ++e) {
+    const float4 val = make_float4(__uint_as_float(v[4 * e]) * scale, __uint_as_float(v[4 * e + 1]) * scale,
+                                   __uint_as_float(v[4 * e + 2]) * scale, __uint_as_float(v[4 * e + 3]) * scale);
+    if (store) dst[e] = val;
+    else atomicAdd(dst + e, val);
+  }
 }
 
-template <int D>
+template <int D, bool kPack>
 __device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const Abort& ab,
                           int t_begin, int t_end) {
   using C = BwdCfg<D>;
@@ -420,13 +456,15 @@ __device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const 
   uint32_t gm = 0, tt = 0;
   for (int i = t_begin; i < t_end; ++i) {
     const BTile t = load_btile(a.tiles, i);
-    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + 1] - a.pb.q_off[t.b]) : a.pb.Lq;
+    // a packed tile is the only one touching its sequences' dQ rows: store
+    const bool packed = kPack && t.n < 0;
+    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + (packed ? -t.n : 1)] - a.pb.q_off[t.b]) : a.pb.Lq;
     const int64_t q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
     for (int m = 0; m < t.qblocks; ++m, ++gm) {
       if (m == t.qblocks - 1) {
         if (!warp_wait_b(smem_u32(&bars.dkv_full), tt & 1, ab)) return;
         tc_fence_after();
-        dkv_epilogue<D>(a, tl, t, r);
+        dkv_epilogue<D, kPack>(a, tl, t, r);
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.dkv_empty));
         ++tt;
@@ -446,7 +484,7 @@ __device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const 
         for (int e = 0; e < 32; ++e) v[32 + e] = w[e];
       }
       if constexpr (D == 128) {
-        if (q_ok) dq_reduce<D>(row, v, a.scale);
+        if (q_ok) dq_out<D>(row, v, a.scale, packed);
         uint32_t w[32];
         tmem_ld_x32(tl + C::kColDP + 64, w);
 #pragma unroll
@@ -456,17 +494,17 @@ __device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const 
         for (int e = 0; e < 32; ++e) v[32 + e] = w[e];
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.dq_empty));  // TMEM released before the last reductions
-        if (q_ok) dq_reduce<D>(row + 64, v, a.scale);
+        if (q_ok) dq_out<D>(row + 64, v, a.scale, packed);
       } else {
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.dq_empty));
-        if (q_ok) dq_reduce<D>(row, v, a.scale);
+        if (q_ok) dq_out<D>(row, v, a.scale, packed);
       }
     }
   }
 }
 
-template <int D>
+template <int D, bool kPack>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     jfa_bwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap do_map,
@@ -516,11 +554,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const Abort ab{&bars.abort_flag, a.status};
   if (warp < 8) {
-    bwd_softmax<D>(a, smem, sbase, tmem, bars, ab, t_begin, t_end, warp >> 2);
+    bwd_softmax<D, kPack>(a, smem, sbase, tmem, bars, ab, t_begin, t_end, warp >> 2);
   } else if (warp >= C::kDrainWarp0) {
-    bwd_drain<D>(a, tmem, bars, ab, t_begin, t_end);
+    bwd_drain<D, kPack>(a, tmem, bars, ab, t_begin, t_end);
   } else if (warp == C::kProducerWarp) {
-    if (lane == 0) bwd_producer<D>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, t_begin, t_end);
+    if (lane == 0) bwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, t_begin, t_end);
     __syncwarp();
   } else {
     if (lane == 0) bwd_mma<D>(a, sbase, tmem, bars, ab, t_begin, t_end);
@@ -534,19 +572,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kPack>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, const CUtensorMap& dO, int grid, cudaStream_t stream) {
   using C = BwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(jfa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(jfa_bwd_kernel<D, kPack>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  jfa_bwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, a);
+  jfa_bwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, a);
   return cudaGetLastError();
 }
 
@@ -569,7 +607,10 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtenso
                        const CUtensorMap& v_map, const CUtensorMap& do_map, int grid,
                        cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  if (a.pb.D == 128) return launch_bwd_d<128>(a, q_map, k_map, v_map, do_map, grid, stream);
-  return launch_bwd_d<64>(a, q_map, k_map, v_map, do_map, grid, stream);
+  if (a.pb.D == 128)
+    return a.packed ? launch_bwd_d<128, true>(a, q_map, k_map, v_map, do_map, grid, stream)
+                    : launch_bwd_d<128, false>(a, q_map, k_map, v_map, do_map, grid, stream);
+  return a.packed ? launch_bwd_d<64, true>(a, q_map, k_map, v_map, do_map, grid, stream)
+                  : launch_bwd_d<64, false>(a, q_map, k_map, v_map, do_map, grid, stream);
 }
 }  // namespace jfa

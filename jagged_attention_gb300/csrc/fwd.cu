@@ -88,7 +88,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kPack>
 __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const CUtensorMap* k_map,
                              const CUtensorMap* v_map, uint32_t sbase, FwdBars& bars,
                              const Abort& ab, int t_begin, int t_end) {
@@ -103,7 +103,7 @@ __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const C
     const Tile t = load_tile(a.tiles, i);
     if (t.cost == 0) continue;
     const int kv0 = a.pb.kv_off[t.b];
-    const int qrow = (a.pb.q_off ? a.pb.q_off[t.b] : 0) + t.blk * 128;
+    const int qrow = (a.pb.q_off ? a.pb.q_off[t.b] : 0) + (kPack ? max(t.blk, 0) : t.blk) * 128;
     const int x0 = t.h * D;
     ok = mbar_wait(smem_u32(&bars.q_empty), (nq & 1) ^ 1, ab);
     if (!ok) break;
@@ -216,7 +216,7 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
 // ---------------------------------------------------------------------------
 // softmax / correction / epilogue (warps 0-3, thread = query row = TMEM lane)
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kPack>
 __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, const Abort& ab,
                             int t_begin, int t_end) {
   using C = FwdCfg<D>;
@@ -229,9 +229,13 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
 
   for (int i = t_begin; i < t_end; ++i) {
     const Tile t = load_tile(a.tiles, i);
-    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + 1] - a.pb.q_off[t.b]) : a.pb.Lq;
-    const int64_t o_first = (a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq) + t.blk * 128;
-    const bool row_ok = int64_t(t.blk) * 128 + r < qlen;
+    // packed tile (blk = -nseq): rows [off[b], off[b + nseq]) of nseq short
+    // sequences, one key block, each row masked to its own sequence's keys
+    const bool packed = kPack && t.blk < 0;
+    const int mblk = packed ? 0 : t.blk;
+    const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + (packed ? -t.blk : 1)] - a.pb.q_off[t.b]) : a.pb.Lq;
+    const int64_t o_first = (a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq) + mblk * 128;
+    const bool row_ok = int64_t(mblk) * 128 + r < qlen;
     const int64_t orow = o_first + r;
     uint16_t* orow_ptr = a.out + (orow * H + t.h) * D;
     if (t.cost == 0) {  // no keys: O = 0, LSE = -inf
@@ -243,7 +247,19 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
       }
       continue;
     }
-    const int last_valid = (a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b]) - (t.cost - 1) * 128;
+    // keys this row may see in the last (peeled) block: [k_lo, k_hi); a
+    // packed tile's single block limits each row to its own sequence
+    int k_lo = 0, k_hi = (a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b]) - (t.cost - 1) * 128;
+    if (packed) {
+      k_hi = 128;  // rows past the pack: never stored
+      if (row_ok) {
+        const int base = a.pb.kv_off[t.b], row = base + r;
+        int sq = t.b;
+        while (a.pb.kv_off[sq + 1] <= row) ++sq;  // the sequence holding this row
+        k_lo = a.pb.kv_off[sq] - base;
+        k_hi = a.pb.kv_off[sq + 1] - base;
+      }
+    }
     float m_run = -INFINITY, l_run = 0.0f, lr_run = 0.0f;  // exact and rounded-weight row sums
     for (int j = 0; j < t.cost; ++j) {
       const uint32_t gj = g + j, sb = gj & 1;
@@ -259,10 +275,16 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.s_empty[sb]));
-      if (j == t.cost - 1 && last_valid < 128) {  // peeled tail: mask keys past the sequence
+      if (j == t.cost - 1) {  // peeled tail: keys outside the sequence
+        if (packed) {
 #pragma unroll
-        for (int e = 0; e < 128; ++e)
-          if (e >= last_valid) s[e] = -INFINITY;
+          for (int e = 0; e < 128; ++e)
+            if (e < k_lo || e >= k_hi) s[e] = -INFINITY;
+        } else if (k_hi < 128) {
+#pragma unroll
+          for (int e = 0; e < 128; ++e)
+            if (e >= k_hi) s[e] = -INFINITY;
+        }
       }
       float mx = s[0];
 #pragma unroll
@@ -342,7 +364,7 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
   }
 }
 
-template <int D>
+template <int D, bool kPack>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
@@ -387,13 +409,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const Abort ab{&bars.abort_flag, a.status};
 
   if (warp == C::kProducerWarp) {
-    if (lane == 0) fwd_producer<D>(a, &q_map, &k_map, &v_map, sbase, bars, ab, t_begin, t_end);
+    if (lane == 0) fwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, sbase, bars, ab, t_begin, t_end);
     __syncwarp();
   } else if (warp == C::kMmaWarp) {
     if (lane == 0) fwd_mma<D>(a, sbase, tmem, bars, ab, t_begin, t_end);
     __syncwarp();
   } else {
-    fwd_softmax<D>(a, tmem, bars, ab, t_begin, t_end);
+    fwd_softmax<D, kPack>(a, tmem, bars, ab, t_begin, t_end);
   }
   tc_fence_before();
   __syncthreads();
@@ -403,19 +425,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kPack>
 cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, kPack>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  jfa_fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, a);
+  jfa_fwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, a);
   return cudaGetLastError();
 }
 
@@ -424,8 +446,13 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorM
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
                        const CUtensorMap& v_map, int grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  if (a.pb.D == 128) return launch_fwd_d<128>(a, q_map, k_map, v_map, grid, stream);
-  return launch_fwd_d<64>(a, q_map, k_map, v_map, grid, stream);
+  // plans with packed short sequences run an instantiation that handles
+  // packed tiles; the others keep the plain code path
+  if (a.pb.D == 128)
+    return a.packed ? launch_fwd_d<128, true>(a, q_map, k_map, v_map, grid, stream)
+                    : launch_fwd_d<128, false>(a, q_map, k_map, v_map, grid, stream);
+  return a.packed ? launch_fwd_d<64, true>(a, q_map, k_map, v_map, grid, stream)
+                  : launch_fwd_d<64, false>(a, q_map, k_map, v_map, grid, stream);
 }
 
 }  // namespace jfa

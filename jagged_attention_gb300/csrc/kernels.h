@@ -24,6 +24,7 @@ struct FwdArgs {
   uint16_t* out;           // bf16 [n_o, H, D]
   float* lse;              // [H, n_o]
   int* status;
+  bool packed;             // the schedule may hold packed tiles {b0, h, -nseq, 1}
 };
 
 struct BwdArgs {
@@ -38,6 +39,7 @@ struct BwdArgs {
   uint16_t* dk;            // bf16 [n_kv, H, D]
   uint16_t* dv;
   int* status;
+  bool packed;             // the schedule may hold packed tiles {b0, h, -nseq, 1}
 };
 
 // Forward: one persistent launch over the schedule (grid = P CTAs).

@@ -28,11 +28,48 @@ bool validate_offsets(const int32_t* off, int B, int64_t* total) {
   return true;
 }
 
+std::vector<int> short_packs(const std::vector<int64_t>& len) {
+  const int B = static_cast<int>(len.size());
+  std::vector<int> pack(B, 1);
+  int b = 0;
+  while (b < B) {
+    if (len[b] == 0 || len[b] > kBM) {
+      ++b;
+      continue;
+    }
+    int64_t total = len[b];
+    int e = b + 1, nonempty = 1;
+    while (e < B && total + len[e] <= kBM) {
+      total += len[e];
+      nonempty += len[e] > 0;
+      ++e;
+    }
+    if (nonempty >= 2) {
+      pack[b] = e - b;
+      for (int i = b + 1; i < e; ++i) pack[i] = 0;
+      b = e;
+    } else {
+      ++b;
+    }
+  }
+  return pack;
+}
+
 Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
-                            int H, int num_ctas) {
+                            int H, int num_ctas, const std::vector<int>* pack) {
   const int B = static_cast<int>(q_len.size());
   std::vector<int32_t> flat;  // enumeration order
   for (int b = 0; b < B; ++b) {
+    if (pack && (*pack)[b] != 1) {
+      if ((*pack)[b] >= 2)
+        for (int h = 0; h < H; ++h) {
+          flat.push_back(b);
+          flat.push_back(h);
+          flat.push_back(-(*pack)[b]);
+          flat.push_back(1);
+        }
+      continue;
+    }
     const int32_t cost = static_cast<int32_t>(cdiv(kv_len[b], kBN));
     const int64_t mblocks = cdiv(q_len[b], kBM);
     for (int h = 0; h < H; ++h)
@@ -70,10 +107,20 @@ Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector
 }
 
 Schedule build_bwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
-                            int H, int num_ctas) {
+                            int H, int num_ctas, const std::vector<int>* pack) {
   const int B = static_cast<int>(q_len.size());
   std::vector<int32_t> flat;
   for (int b = 0; b < B; ++b) {
+    if (pack && (*pack)[b] != 1) {
+      if ((*pack)[b] >= 2)
+        for (int h = 0; h < H; ++h) {
+          flat.push_back(b);
+          flat.push_back(h);
+          flat.push_back(-(*pack)[b]);
+          flat.push_back(1);
+        }
+      continue;
+    }
     if (q_len[b] == 0) continue;
     const int32_t qblocks = static_cast<int32_t>(cdiv(q_len[b], kBM));
     const int64_t nblocks = cdiv(kv_len[b], kBN);

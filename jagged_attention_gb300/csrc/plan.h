@@ -22,21 +22,31 @@ struct Schedule {
 // total through *total.  false on any violation.
 bool validate_offsets(const int32_t* off, int B, int64_t* total);
 
+// Packing of short sequences (self mode with one shared offsets array): a run
+// of consecutive sequences whose lengths add up to at most 128 rows, with at
+// least two non-empty ones, becomes one tile {b0, h, -nseq, 1} covering rows
+// [off[b0], off[b0 + nseq]) with a block-diagonal mask.  pack[b] is nseq for a
+// pack starting at b, 0 for a sequence inside a pack, and 1 otherwise.
+std::vector<int> short_packs(const std::vector<int64_t>& len);
+
 // Forward schedule: tiles (b, h, m) for m < ceil(Lq_b / BM) with cost
 // ceil(Lk_b / BN), stable-sorted by cost descending, dealt zigzag to
 // P = min(num_ctas, T) CTAs.
+// `pack` (optional) replaces packed runs by one tile each.
 Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
-                            int H, int num_ctas);
+                            int H, int num_ctas, const std::vector<int>* pack = nullptr);
 // Backward schedule: tiles (b, h, n) for n < ceil(Lk_b / BN) where Lq_b > 0,
 // cost ceil(Lq_b / BM), dealt round-robin.
 Schedule build_bwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
-                            int H, int num_ctas);
+                            int H, int num_ctas, const std::vector<int>* pack = nullptr);
 
 }  // namespace jfa
 
 struct jfa_plan {
   int B = 0, H = 0, Lq = 0, D = 0;
   bool broadcast = false;
+  bool packed = false;       // short sequences packed into shared tiles
+  bool all_packed = false;   // every sequence with rows sits in a packed tile
   int device = 0;
   int num_ctas = 0;
   int64_t n_q = 0;   // rows of Q

@@ -26,6 +26,15 @@ Readings where the pages leave the details open:
 
 Every tile is four int32: (b, h, blk, cost).  The result is CSR: ``tiles``
 [T, 4] grouped by CTA and ``cta_ptr`` [P + 1].
+
+Optional packing of short sequences (the block-diagonal case of the TLX Block
+Attention page, "One Constraint, Five Eliminations": a 64-token segment only
+attends within itself), for self mode with one shared offsets array: scanning
+b upward, a sequence of length 1..128 starts a run that greedily takes the
+following sequences while the run's total stays within 128 rows; a run with
+at least two non-empty sequences becomes one tile (b0, h, -nseq, 1) per head
+and replaces those sequences' own tiles (forward cost 1, backward 1 query
+block); other sequences keep their ordinary tiles.
 """
 from __future__ import annotations
 
@@ -36,9 +45,38 @@ def _ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-def fwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int):
+def short_packs(lengths, limit: int = 128):
+    """pack[b]: run length for a run starting at b, 0 inside a run, 1 otherwise."""
+    B = len(lengths)
+    pack = [1] * B
+    b = 0
+    while b < B:
+        L = int(lengths[b])
+        if L == 0 or L > limit:
+            b += 1
+            continue
+        total, e, nonempty = L, b + 1, 1
+        while e < B and total + int(lengths[e]) <= limit:
+            total += int(lengths[e])
+            nonempty += int(lengths[e]) > 0
+            e += 1
+        if nonempty >= 2:
+            pack[b] = e - b
+            for i in range(b + 1, e):
+                pack[i] = 0
+            b = e
+        else:
+            b += 1
+    return pack
+
+
+def fwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pack=None):
     tiles = []
     for b in range(len(q_lengths)):
+        if pack is not None and pack[b] != 1:
+            if pack[b] >= 2:
+                tiles.extend((b, h, -pack[b], 1) for h in range(H))
+            continue
         cost = _ceil_div(int(kv_lengths[b]), BN)
         for h in range(H):
             for m in range(_ceil_div(int(q_lengths[b]), BM)):
@@ -54,9 +92,13 @@ def fwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int):
     return _csr(per_cta, P)
 
 
-def bwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int):
+def bwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pack=None):
     tiles = []
     for b in range(len(q_lengths)):
+        if pack is not None and pack[b] != 1:
+            if pack[b] >= 2:
+                tiles.extend((b, h, -pack[b], 1) for h in range(H))
+            continue
         if int(q_lengths[b]) == 0:
             continue
         qblocks = _ceil_div(int(q_lengths[b]), BM)

@@ -23,8 +23,8 @@ def to_cuda(p: workloads.Problem) -> workloads.Problem:
                              p.q.cuda(), p.k.cuda(), p.v.cuda(), p.dout.cuda(), p.scale)
 
 
-def make_plan(p: workloads.Problem, num_ctas: int = 0) -> jfa.Plan:
-    return jfa.Plan(p.kv_offsets, p.q_offsets, H=p.H, D=p.D, Lq=p.Lq, num_ctas=num_ctas)
+def make_plan(p: workloads.Problem, num_ctas: int = 0, flags: int = 0) -> jfa.Plan:
+    return jfa.Plan(p.kv_offsets, p.q_offsets, H=p.H, D=p.D, Lq=p.Lq, num_ctas=num_ctas, flags=flags)
 
 
 def gpu_fwd(p: workloads.Problem, plan: jfa.Plan | None = None):

@@ -25,9 +25,9 @@ def test_exports_every_declared_function():
         assert hasattr(L, n), n
 
 
-def _ref(qlen, klen, H, P, direction):
+def _ref(qlen, klen, H, P, direction, pack=None):
     fn = ref_tiles.fwd_tiles if direction == 0 else ref_tiles.bwd_tiles
-    return fn(qlen, klen, H, 128, 128, P)
+    return fn(qlen, klen, H, 128, 128, P, pack)
 
 
 @pytest.mark.parametrize("case", load_cases(), ids=lambda c: c["name"])
@@ -38,7 +38,8 @@ def test_native_builder_matches_hand_worked(case):
     qo = None if bcast else workloads.offsets_from_lengths(ql)
     Lq = int(ql[0]) if bcast else 0
     for d, key in ((0, "fwd"), (1, "bwd")):
-        t, p = jfa.build_tiles(kv, qo, H=case["H"], Lq=Lq, num_ctas=case["num_ctas"], direction=d)
+        t, p = jfa.build_tiles(kv, qo, H=case["H"], Lq=Lq, num_ctas=case["num_ctas"], direction=d,
+                               flags=case.get("flags", 0))
         assert np.array_equal(t, case[key]) and np.array_equal(p, case[f"{key}_cta_ptr"])
 
 
@@ -78,6 +79,36 @@ def test_native_builder_matches_reference_on_workloads(name):
         assert np.array_equal(t, rt) and np.array_equal(p, rp)
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_native_packed_builder_matches_reference_random(seed):
+    rng = np.random.default_rng(300 + seed)
+    B = int(rng.integers(1, 80))
+    H = int(rng.integers(1, 4))
+    lens = rng.integers(0, 140, size=B)
+    lens[rng.random(B) < 0.2] = int(rng.integers(129, 600))
+    lens[rng.random(B) < 0.1] = 0
+    kv = workloads.offsets_from_lengths(lens)
+    P = int(rng.integers(1, 100))
+    pack = ref_tiles.short_packs(lens)
+    for d in (0, 1):
+        t, p = jfa.build_tiles(kv, kv, H=H, num_ctas=P, direction=d, flags=jfa.PLAN_PACK_SHORT)
+        rt, rp = _ref(lens, lens, H, P, d, pack)
+        assert np.array_equal(t, rt) and np.array_equal(p, rp)
+    # different query offsets or broadcast mode: the flag is ignored
+    t, _ = jfa.build_tiles(kv, kv.copy() + 0, H=H, num_ctas=P, direction=0, flags=jfa.PLAN_PACK_SHORT)
+    t0, _ = jfa.build_tiles(kv, None, H=H, Lq=64, num_ctas=P, direction=0, flags=jfa.PLAN_PACK_SHORT)
+    assert np.array_equal(t0, _ref(np.full(B, 64), lens, H, P, 0)[0])
+
+
+def test_packed_block_diagonal_workload_halves_the_tiles():
+    w = workloads.WORKLOADS["block_diag"]
+    kv = workloads.offsets_from_lengths(workloads.draw_lengths(w.lengths, w.B, 0))
+    plain = jfa.build_tiles(kv, kv, H=w.H, num_ctas=152, direction=0)[0]
+    packed = jfa.build_tiles(kv, kv, H=w.H, num_ctas=152, direction=0, flags=jfa.PLAN_PACK_SHORT)[0]
+    assert packed.shape[0] * 2 == plain.shape[0]
+    assert (packed[:, 2] == -2).all() and (packed[:, 3] == 1).all()
+
+
 def test_seed0_tile_counts():
     # tile totals of the five workloads at seed 0
     want = {"tiny_broadcast": (8, 8), "jagged_self": (624, 624), "gem_broadcast": (8192, 26028),
@@ -114,10 +145,10 @@ def test_rejects_bad_arguments_before_touching_the_device():
     L = jfa.lib()
     T, P = ctypes.c_int(), ctypes.c_int()
     kv = np.array([0, 4, 2], dtype=np.int32)
-    assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 0, None, None,
+    assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 0, 0, None, None,
                              ctypes.byref(T), ctypes.byref(P)) == 3
     kv = np.array([0, 4, 6], dtype=np.int32)
-    assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 2, None, None,
+    assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 2, 0, None, None,
                              ctypes.byref(T), ctypes.byref(P)) == 1  # bad direction
     assert L.jfa_fwd(None, None, None, None, 1.0, None, None, None) == 1
     assert L.jfa_bwd(None, None, None, None, None, None, None, 1.0, None, None, None, None, 0,

@@ -16,9 +16,9 @@ def _built():
     jfa.build()
 
 
-def _run(p, num_ctas=0):
+def _run(p, num_ctas=0, flags=0):
     p = parity.to_cuda(p)
-    plan = parity.make_plan(p, num_ctas)
+    plan = parity.make_plan(p, num_ctas, flags)
     out, lse, _ = parity.gpu_fwd(p, plan)
     dq, dk, dv = parity.gpu_bwd(p, out, lse, plan)
     rdq, rdk, rdv = parity.oracle_bwd(p)
@@ -75,3 +75,18 @@ def test_dk_dv_deterministic():
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     # dQ is reduce-added in arbitrary order: equal up to fp32 rounding
     assert (a[0] - b[0]).abs().max().item() <= 1e-5 * max(1.0, a[0].abs().max().item())
+
+
+PACKED_LENGTHS = [60, 40, 30, 200, 64, 64, 1, 1, 0, 127, 1, 5, 0, 0, 33, 95]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_packed_short_sequences(D):
+    import jagged_attention_gb300 as jfa
+    _run(workloads.make_problem(len(PACKED_LENGTHS), 2, D, "self", PACKED_LENGTHS, seed=20),
+         flags=jfa.PLAN_PACK_SHORT)
+
+
+def test_packed_block_diagonal_segments():
+    import jagged_attention_gb300 as jfa
+    _run(workloads.make_problem(24, 2, 128, "self", [64] * 24, seed=21), flags=jfa.PLAN_PACK_SHORT)

@@ -36,13 +36,14 @@ def _sampled_sequences(p, rng, n_random=3):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("name", ["gem_broadcast", "skewed_broadcast", "block_diag"])
-def test_full_size_sampled_parity(name):
+@pytest.mark.parametrize("name,flags", [("gem_broadcast", 0), ("skewed_broadcast", 0),
+                                        ("block_diag", 0), ("block_diag", 1)])
+def test_full_size_sampled_parity(name, flags):
     torch.cuda.empty_cache()
     orc = oracle.default()
     rng = np.random.default_rng(123)
     p = workloads.make_workload(name, seed=0, device="cuda")
-    plan = parity.make_plan(p)              # num_ctas = SM count, as bench.py runs it
+    plan = parity.make_plan(p, flags=flags)  # num_ctas = SM count, as bench.py runs it
     out, lse, _ = parity.gpu_fwd(p, plan)
     dq, dk, dv = parity.gpu_bwd(p, out, lse, plan)
 

@@ -18,9 +18,9 @@ def _built():
     jfa.build()
 
 
-def _run(p, num_ctas=0):
+def _run(p, num_ctas=0, flags=0):
     p = parity.to_cuda(p)
-    out, lse, plan = parity.gpu_fwd(p, parity.make_plan(p, num_ctas))
+    out, lse, plan = parity.gpu_fwd(p, parity.make_plan(p, num_ctas, flags))
     O_ref, L_ref = parity.oracle_fwd(p)
     return parity.check_fwd(out, lse, O_ref, L_ref)
 
@@ -99,3 +99,18 @@ def test_repeated_calls_are_deterministic():
     o1, l1, _ = parity.gpu_fwd(p, plan)
     o2, l2, _ = parity.gpu_fwd(p, plan)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+PACKED_LENGTHS = [60, 40, 30, 200, 64, 64, 1, 1, 0, 127, 1, 5, 0, 0, 33, 95]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_packed_short_sequences(D):
+    import jagged_attention_gb300 as jfa
+    _run(workloads.make_problem(len(PACKED_LENGTHS), 2, D, "self", PACKED_LENGTHS, seed=20),
+         flags=jfa.PLAN_PACK_SHORT)
+
+
+def test_packed_block_diagonal_segments():
+    import jagged_attention_gb300 as jfa
+    _run(workloads.make_problem(24, 2, 128, "self", [64] * 24, seed=21), flags=jfa.PLAN_PACK_SHORT)

@@ -11,8 +11,9 @@ BM = BN = 128
 
 @pytest.mark.parametrize("case", load_cases(), ids=lambda c: c["name"])
 def test_reference_builder_matches_hand_worked(case):
-    ft, fp = tiles.fwd_tiles(case["q_lengths"], case["kv_lengths"], case["H"], BM, BN, case["num_ctas"])
-    bt, bp = tiles.bwd_tiles(case["q_lengths"], case["kv_lengths"], case["H"], BM, BN, case["num_ctas"])
+    pack = tiles.short_packs(case["kv_lengths"]) if case.get("flags", 0) else None
+    ft, fp = tiles.fwd_tiles(case["q_lengths"], case["kv_lengths"], case["H"], BM, BN, case["num_ctas"], pack)
+    bt, bp = tiles.bwd_tiles(case["q_lengths"], case["kv_lengths"], case["H"], BM, BN, case["num_ctas"], pack)
     assert np.array_equal(fp, case["fwd_cta_ptr"]) and np.array_equal(ft, case["fwd"])
     assert np.array_equal(bp, case["bwd_cta_ptr"]) and np.array_equal(bt, case["bwd"])
 
@@ -61,3 +62,39 @@ def test_schedule_properties(seed):
 def test_empty_problem():
     ft, fp = tiles.fwd_tiles([0, 0], [5, 0], 2, BM, BN, 8)
     assert ft.shape == (0, 4) and list(fp) == [0]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_packed_schedule_properties(seed):
+    rng = np.random.default_rng(50 + seed)
+    B = int(rng.integers(1, 60))
+    lens = rng.integers(0, 150, size=B)
+    lens[rng.random(B) < 0.2] = 0
+    pack = tiles.short_packs(lens)
+    # packs cover consecutive sequences, fit one tile and hold >= 2 non-empty sequences
+    covered = set()
+    for b, n in enumerate(pack):
+        if n >= 2:
+            assert sum(int(x) for x in lens[b:b + n]) <= 128
+            assert sum(int(x) > 0 for x in lens[b:b + n]) >= 2
+            assert all(pack[i] == 0 for i in range(b + 1, b + n))
+            covered.update(range(b, b + n))
+        elif n == 0:
+            assert b in covered
+    ft, fp = tiles.fwd_tiles(lens, lens, 2, BM, BN, 7, pack)
+    rows = {}
+    for b, h, blk, cost in ft:
+        if blk < 0:
+            seqs = range(b, b - blk)
+        else:
+            seqs = [b]
+        for s in seqs:
+            rows.setdefault((s, h), 0)
+            rows[(s, h)] += 1 if blk < 0 else 0
+    # every non-empty sequence is either packed once per head or tiled normally
+    for b in range(B):
+        if lens[b] == 0:
+            continue
+        for h in range(2):
+            if b in covered:
+                assert rows[(b, h)] == 1
