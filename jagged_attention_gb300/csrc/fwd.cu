@@ -15,9 +15,12 @@
 // (alphasignal page, "Specialized warps keep tensor cores busy": a load warp,
 // an MMA warp, softmax/correction warps, output stores; a multi-stage K/V
 // pipeline; persistent CTAs), re-derived for sm_103a:
-//   warp 4      TMA producer (Q once per tile, K and V per block)
-//   warp 5      tcgen05.mma issuer; owns the TMEM allocation
-//   warps 0-3   softmax + correction + epilogue, one thread per query row
+//   warp 8      TMA producer (Q once per tile, K and V per block)
+//   warp 9      tcgen05.mma issuer; owns the TMEM allocation
+//   warps 0-3,  softmax + correction + epilogue: two groups share every query
+//   warps 4-7   row (key columns [0, 64) and [64, 128) of each block, O
+//               columns [0, D/2) and [D/2, D)) and exchange row maxima and
+//               sums through shared memory
 // TMEM (512 columns): two 128-column score buffers (so QK^T of block j+1
 // overlaps the softmax of block j), the D-column O accumulator and two
 // 64-column bf16 P buffers.  O is rescaled only when a row's max grows by
@@ -38,19 +41,25 @@ struct FwdCfg {
   static constexpr int kChunks = D / 64;             // 128-byte column chunks per row
   static constexpr int kChunkBytes = 128 * 128;      // one [128 rows x 64 bf16] chunk
   static constexpr int kTileBytes = 128 * D * 2;     // one 128-row tile of Q, K or V
-  static constexpr int kStages = (D == 128) ? 3 : 4; // K and V ring depth (keeps 1 CTA/SM)
+  static constexpr int kStages = (D == 128) ? 2 : 4; // K and V ring depth (keeps 1 CTA/SM)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+  // row statistics the two softmax groups exchange: per-block partial maxima
+  // (2 buffers x 2 groups x 128 rows) and per-tile partial sums (2 buffers x
+  // 2 groups x 2 sums x 128 rows)
+  static constexpr int kOffXMax = kOffV + kStages * kTileBytes;
+  static constexpr int kOffXSum = kOffXMax + 2 * 2 * 128 * 4;
+  static constexpr int kOffBar = kOffXSum + 2 * 2 * 2 * 128 * 4;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + barriers + alignment slack
   static constexpr uint32_t kColS = 0;               // 2 x 128 fp32 columns
   static constexpr uint32_t kColO = 256;             // D fp32 columns
   static constexpr uint32_t kColP = 256 + D;         // 2 x 64 columns of bf16 pairs
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 192;
-  static constexpr int kProducerWarp = 4;
-  static constexpr int kMmaWarp = 5;
+  static constexpr int kThreads = 320;
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;
 };
 
 struct FwdBars {
@@ -58,6 +67,8 @@ struct FwdBars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
   uint64_t o_empty;
+  uint64_t max_ready[2];  // both groups' partial row maxima of a block are in shared memory
+  uint64_t sum_ready[2];  // both groups' partial row sums of a tile are in shared memory
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -217,15 +228,19 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
 // softmax / correction / epilogue (warps 0-3, thread = query row = TMEM lane)
 // ---------------------------------------------------------------------------
 template <int D, bool kPack>
-__device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, const Abort& ab,
-                            int t_begin, int t_end) {
+__device__ void fwd_softmax(const FwdArgs& a, uint8_t* smem, uint32_t tmem, FwdBars& bars,
+                            const Abort& ab, int t_begin, int t_end, int grp) {
   using C = FwdCfg<D>;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int r = tid;  // row of the tile, TMEM lane
-  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = (warp & 3) * 32 + lane;  // row of the tile, TMEM lane
+  const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const int c0 = 64 * grp;               // this group's key columns in a block
+  const int o0 = grp * (D / 2);          // and O columns
+  float* xmax = reinterpret_cast<float*>(smem + C::kOffXMax);  // [2][2][128]
+  float* xsum = reinterpret_cast<float*>(smem + C::kOffXSum);  // [2][2][2][128]
   const float sl2 = a.scale_log2;
   const int H = a.pb.H;
-  uint32_t g = 0;
+  uint32_t g = 0, tq = 0;
 
   for (int i = t_begin; i < t_end; ++i) {
     const Tile t = load_tile(a.tiles, i);
@@ -237,13 +252,13 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
     const int64_t o_first = (a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq) + mblk * 128;
     const bool row_ok = int64_t(mblk) * 128 + r < qlen;
     const int64_t orow = o_first + r;
-    uint16_t* orow_ptr = a.out + (orow * H + t.h) * D;
+    uint16_t* orow_ptr = a.out + (orow * H + t.h) * D + o0;
     if (t.cost == 0) {  // no keys: O = 0, LSE = -inf
       if (row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(orow_ptr);
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-        a.lse[int64_t(t.h) * a.pb.n_o + orow] = -INFINITY;
+        for (int c = 0; c < D / 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        if (grp == 0) a.lse[int64_t(t.h) * a.pb.n_o + orow] = -INFINITY;
       }
       continue;
     }
@@ -260,16 +275,18 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
         k_hi = a.pb.kv_off[sq + 1] - base;
       }
     }
-    float m_run = -INFINITY, l_run = 0.0f, lr_run = 0.0f;  // exact and rounded-weight row sums
+    // the group's partial sums (exact and of the bf16-rounded weights); the
+    // running max is the same in both groups (they combine their maxima)
+    float m_run = -INFINITY, l_run = 0.0f, lr_run = 0.0f;
     for (int j = 0; j < t.cost; ++j) {
       const uint32_t gj = g + j, sb = gj & 1;
       if (!warp_wait(smem_u32(&bars.s_full[sb]), (gj >> 1) & 1, ab)) return;
       tc_fence_after();
-      float s[128];
+      float s[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld_x32(tl + C::kColS + sb * 128 + c * 32, v);
+        tmem_ld_x32(tl + C::kColS + sb * 128 + c0 + c * 32, v);
 #pragma unroll
         for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
       }
@@ -278,25 +295,31 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
       if (j == t.cost - 1) {  // peeled tail: keys outside the sequence
         if (packed) {
 #pragma unroll
-          for (int e = 0; e < 128; ++e)
-            if (e < k_lo || e >= k_hi) s[e] = -INFINITY;
+          for (int e = 0; e < 64; ++e)
+            if (c0 + e < k_lo || c0 + e >= k_hi) s[e] = -INFINITY;
         } else if (k_hi < 128) {
 #pragma unroll
-          for (int e = 0; e < 128; ++e)
-            if (e >= k_hi) s[e] = -INFINITY;
+          for (int e = 0; e < 64; ++e)
+            if (c0 + e >= k_hi) s[e] = -INFINITY;
         }
       }
       float mx = s[0];
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, s[e]);
+      for (int e = 1; e < 64; ++e) mx = fmaxf(mx, s[e]);
+      // combine with the other group's maximum of this row
+      float* xm = xmax + (gj & 1) * 256;
+      xm[grp * 128 + r] = mx;
+      mbar_arrive(smem_u32(&bars.max_ready[gj & 1]));
+      if (!warp_wait(smem_u32(&bars.max_ready[gj & 1]), (gj >> 1) & 1, ab)) return;
+      mx = fmaxf(mx, xm[(grp ^ 1) * 128 + r]);
       const float m_cand = mx * sl2;
       const bool resc = m_cand > m_run + kRescaleThreshold;
       const float m_new = resc ? m_cand : m_run;
       const float alpha = resc ? fast_exp2(m_run - m_new) : 1.0f;
-      uint32_t p[64];
+      uint32_t p[32];
       float rowsum = 0.0f, rowsum_r = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
+      for (int e = 0; e < 32; ++e) {
         const float p0 = fast_exp2(fmaf(s[2 * e], sl2, -m_new));
         const float p1 = fast_exp2(fmaf(s[2 * e + 1], sl2, -m_new));
         p[e] = pack_bf16x2(p0, p1);
@@ -315,38 +338,38 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
         if (!warp_wait(smem_u32(&bars.pv_done[gp & 1]), (gp >> 1) & 1, ab)) return;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
-          tmem_ld_x32(tl + C::kColO + c * 32, v);
+          tmem_ld_x32(tl + C::kColO + o0 + c * 32, v);
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st_x32(tl + C::kColO + c * 32, v);
+          tmem_st_x32(tl + C::kColO + o0 + c * 32, v);
         }
       }
-      {
-        uint32_t lo[32], hi[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          lo[e] = p[e];
-          hi[e] = p[32 + e];
-        }
-        tmem_st_x32(tl + C::kColP + sb * 64, lo);
-        tmem_st_x32(tl + C::kColP + sb * 64 + 32, hi);
-      }
+      // P of key columns [c0, c0 + 64) = packed columns [32 grp, 32 grp + 32)
+      tmem_st_x32(tl + C::kColP + sb * 64 + grp * 32, p);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full[sb]));
       m_run = m_new;
     }
-    // epilogue: wait for the last PV, normalise, store O and LSE
+    // epilogue: combine the groups' row sums, wait for the last PV,
+    // normalise this group's O columns, store O and LSE
+    float* xs = xsum + (tq & 1) * 512;  // [group][exact, rounded][128]
+    xs[grp * 256 + r] = l_run;
+    xs[grp * 256 + 128 + r] = lr_run;
+    mbar_arrive(smem_u32(&bars.sum_ready[tq & 1]));
+    if (!warp_wait(smem_u32(&bars.sum_ready[tq & 1]), (tq >> 1) & 1, ab)) return;
+    l_run += xs[(grp ^ 1) * 256 + r];
+    lr_run += xs[(grp ^ 1) * 256 + 128 + r];
     const uint32_t gl = g + t.cost - 1;
     if (!warp_wait(smem_u32(&bars.pv_done[gl & 1]), (gl >> 1) & 1, ab)) return;
     tc_fence_after();
     const float inv_l = 1.0f / lr_run;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < D / 64; ++c) {
       uint32_t v[32];
-      tmem_ld_x32(tl + C::kColO + c * 32, v);
+      tmem_ld_x32(tl + C::kColO + o0 + c * 32, v);
       if (row_ok) {
         uint32_t w[16];
 #pragma unroll
@@ -359,8 +382,9 @@ __device__ void fwd_softmax(const FwdArgs& a, uint32_t tmem, FwdBars& bars, cons
     }
     tc_fence_before();
     mbar_arrive(smem_u32(&bars.o_empty));
-    if (row_ok) a.lse[int64_t(t.h) * a.pb.n_o + orow] = (m_run + __log2f(l_run)) * kLn2;
+    if (row_ok && grp == 0) a.lse[int64_t(t.h) * a.pb.n_o + orow] = (m_run + __log2f(l_run)) * kLn2;
     g += t.cost;
+    ++tq;
   }
 }
 
@@ -389,11 +413,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.s_full[s]), 1);
-      mbar_init(smem_u32(&bars.s_empty[s]), 128);
-      mbar_init(smem_u32(&bars.p_full[s]), 128);
+      mbar_init(smem_u32(&bars.s_empty[s]), 256);
+      mbar_init(smem_u32(&bars.p_full[s]), 256);
+      mbar_init(smem_u32(&bars.max_ready[s]), 256);
+      mbar_init(smem_u32(&bars.sum_ready[s]), 256);
       mbar_init(smem_u32(&bars.pv_done[s]), 1);
     }
-    mbar_init(smem_u32(&bars.o_empty), 128);
+    mbar_init(smem_u32(&bars.o_empty), 256);
     mbar_init(smem_u32(&bars.drain), 1);
     bars.abort_flag = 0;
     fence_mbar_init();
@@ -415,7 +441,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     if (lane == 0) fwd_mma<D>(a, sbase, tmem, bars, ab, t_begin, t_end);
     __syncwarp();
   } else {
-    fwd_softmax<D, kPack>(a, tmem, bars, ab, t_begin, t_end);
+    fwd_softmax<D, kPack>(a, smem, tmem, bars, ab, t_begin, t_end, warp >> 2);
   }
   tc_fence_before();
   __syncthreads();
@@ -430,6 +456,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorM
                          const CUtensorMap& v, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
+  static_assert(sizeof(FwdBars) <= C::kBarBytes, "barrier block");
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, kPack>,
