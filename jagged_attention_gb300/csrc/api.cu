@@ -53,6 +53,24 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
   return r == CUDA_SUCCESS ? JFA_OK : JFA_ERR_CUDA;
 }
 
+// TMA descriptor of the fp32 dQ viewed as 2-D [rows, H*D]: boxes of 32 rows x
+// 32 columns (128 bytes, 128-byte swizzle), the unit one warp of the backward
+// reduce-adds (or stores) from shared memory.  Out-of-range rows are skipped.
+int make_map_dq(CUtensorMap* m, const float* ptr, int64_t rows, int64_t cols) {
+  std::memset(m, 0, sizeof(*m));
+  if (rows == 0) return JFA_OK;
+  auto enc = tensor_map_encoder();
+  if (!enc) return JFA_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? JFA_OK : JFA_ERR_CUDA;
+}
+
 jfa::Problem problem_of(const jfa_plan* p) {
   jfa::Problem pb;
   pb.kv_off = p->d_kv_off;
@@ -343,9 +361,10 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
     return JFA_ERR_WORKSPACE;
   if (plan->bwd.P == 0) return JFA_OK;
   const int64_t cols = int64_t(plan->H) * plan->D;
-  CUtensorMap qm, km, vm, dom;
+  CUtensorMap qm, km, vm, dom, dqm;
   if (make_map(&qm, q, plan->n_q, cols) || make_map(&km, k, plan->n_kv, cols) ||
-      make_map(&vm, v, plan->n_kv, cols) || make_map(&dom, dout, plan->n_o, cols))
+      make_map(&vm, v, plan->n_kv, cols) || make_map(&dom, dout, plan->n_o, cols) ||
+      make_map_dq(&dqm, dq, plan->n_q, cols))
     return JFA_ERR_CUDA;
   jfa::BwdArgs a;
   a.pb = problem_of(plan);
@@ -360,7 +379,8 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
   a.dv = static_cast<uint16_t*>(dv);
   a.status = plan->d_status;
   a.packed = plan->packed;
-  cudaError_t e = jfa::launch_bwd(a, qm, km, vm, dom, plan->bwd.P, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      jfa::launch_bwd(a, qm, km, vm, dom, dqm, plan->bwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
@@ -479,9 +499,9 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   cudaError_t e = jfa::launch_delta(static_cast<const uint16_t*>(out),
                                     static_cast<const uint16_t*>(dout), delta, n_o, H, D, s);
   if (e != cudaSuccess) return JFA_ERR_CUDA;
-  CUtensorMap qm, km, vm, dom;
+  CUtensorMap qm, km, vm, dom, dqm;
   if (make_map(&qm, q, n_q, cols) || make_map(&km, k, n_kv, cols) || make_map(&vm, v, n_kv, cols) ||
-      make_map(&dom, dout, n_o, cols))
+      make_map(&dom, dout, n_o, cols) || make_map_dq(&dqm, dq, n_q, cols))
     return JFA_ERR_CUDA;
   jfa::BwdArgs a;
   a.pb.kv_off = reinterpret_cast<const int32_t*>(scratch + o_kv);
@@ -504,7 +524,7 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   a.dv = static_cast<uint16_t*>(dv);
   a.status = device_status ? device_status : reinterpret_cast<int*>(scratch + o_st);
   a.packed = false;
-  e = jfa::launch_bwd(a, qm, km, vm, dom, sched.P, s);
+  e = jfa::launch_bwd(a, qm, km, vm, dom, dqm, sched.P, s);
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

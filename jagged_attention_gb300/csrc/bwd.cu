@@ -257,9 +257,8 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
         mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sDS + kk * 2048, C::kChunkBytes, 1024),
                     smem_desc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), id_dq,
                     kk > 0 ? 1u : 0u);
-      mma_commit(smem_u32(&bars.dq_full));
+      mma_commit(smem_u32(&bars.dq_full));  // also: Q/dO stage qs read for the last time
       mma_commit(smem_u32(&bars.ds_empty));
-      mma_commit(smem_u32(&bars.q_empty[qs]));
       if (m == t.qblocks - 1) {
         mma_commit(smem_u32(&bars.dkv_full));
         mma_commit(smem_u32(&bars.kv_empty[kb]));  // K read for the last time
@@ -394,13 +393,12 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
 }
 
 // ---------------------------------------------------------------------------
-// Drain group (warps 10-13): dQ_m leaves TMEM (thread = query row) in two
-// passes of 64 columns, the TMEM columns are released as soon as the slice is
-// in registers, and the fp32 vector reduce-adds into dq follow (the cross-batch
-// reduction of the broadcast mode happens here, in the memory system).  At the
-// end of a tile the group writes dV and scale * dK (thread = key row) before
-// the tile's last dQ reductions, so the next tile's products do not wait for
-// them.
+// Drain group (warps 10-13): dQ_m leaves TMEM (thread = query row), the TMEM
+// columns are released as soon as it is in shared memory, and tensor reduce-adds
+// into dq follow (the cross-batch reduction of the broadcast mode happens
+// here, in the memory system).  At the end of a tile the group writes dV and
+// scale * dK (thread = key row) before the tile's last dQ, so the next tile's
+// products do not wait for them.
 template <int D, bool kPack>
 __device__ __forceinline__ void dkv_epilogue(const BwdArgs& a, uint32_t tl, const BTile& t, int r) {
   using C = BwdCfg<D>;
@@ -432,12 +430,11 @@ __device__ __forceinline__ void dkv_epilogue(const BwdArgs& a, uint32_t tl, cons
   }
 }
 
-// 64 dQ columns of one row: reduce-added, or stored when this tile owns the row.
-template <int D>
-__device__ __forceinline__ void dq_out(float* row, const uint32_t (&v)[64], float scale, bool store) {
+// 32 dQ columns of one row: reduce-added, or stored when this tile owns the row.
+__device__ __forceinline__ void dq_row_out(float* row, const uint32_t (&v)[32], float scale, bool store) {
   float4* dst = reinterpret_cast<float4*>(row);
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
+  for (int e = 0; e < 8; ++e) {
     const float4 val = make_float4(__uint_as_float(v[4 * e]) * scale, __uint_as_float(v[4 * e + 1]) * scale,
                                    __uint_as_float(v[4 * e + 2]) * scale, __uint_as_float(v[4 * e + 3]) * scale);
     if (store) dst[e] = val;
@@ -445,13 +442,23 @@ __device__ __forceinline__ void dq_out(float* row, const uint32_t (&v)[64], floa
   }
 }
 
+// dQ leaves TMEM a thread per query row, but the memory system takes row-wise
+// scattered 16-byte pieces at a fraction of the rate of whole rows.  So each
+// drain warp writes its 32 rows into shared memory in the 128-byte-swizzled
+// box layout and hands them to the tensor-memory-access unit as D/32 boxes of
+// 32 x 32 fp32 (reduce-add, or store for packed tiles).  The staging space is
+// the Q/dO stage of the step just finished, free once dq_full has fired: its
+// D/32 boxes of 16 KB fill the Q stage first, then the dO stage.  The stage
+// returns to the producer when every drain warp's boxes have been read out.
+// A warp whose rows run past the sequence writes its valid rows directly.
 template <int D, bool kPack>
-__device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const Abort& ab,
-                          int t_begin, int t_end) {
+__device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, uint32_t sbase,
+                          uint32_t tmem, BwdBars& bars, const Abort& ab, int t_begin, int t_end) {
   using C = BwdCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = (warp & 3) * 32 + lane;  // TMEM lane of this thread
-  const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;  // TMEM lane of this thread
+  const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const int H = a.pb.H;
   uint32_t gm = 0, tt = 0;
   for (int i = t_begin; i < t_end; ++i) {
@@ -471,35 +478,50 @@ __device__ void bwd_drain(const BwdArgs& a, uint32_t tmem, BwdBars& bars, const 
       }
       if (!warp_wait_b(smem_u32(&bars.dq_full), gm & 1, ab)) return;
       tc_fence_after();
+      const uint32_t qs = gm & 1;
       const bool q_ok = int64_t(m) * 128 + r < qlen;
+      const bool whole = __all_sync(0xffffffffu, q_ok);
       float* row = a.dq + ((q_base + int64_t(m) * 128 + r) * H + t.h) * D;
-      uint32_t v[64];
-      {
-        uint32_t w[32];
-        tmem_ld_x32(tl + C::kColDP, w);
+      auto box_addr = [&](int k) -> uint32_t {  // this warp's 32 rows of box k
+        return sbase + (k < D / 64 ? C::kOffQ + qs * C::kTileBytes + k * 16384
+                                   : C::kOffDO + qs * C::kTileBytes + (k - D / 64) * 16384) +
+               wq * 4096;
+      };
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = w[e];
-        tmem_ld_x32(tl + C::kColDP + 32, w);
+      for (int k = 0; k < D / 32; ++k) {
+        uint32_t v[32];
+        tmem_ld_x32(tl + C::kColDP + k * 32, v);
+        if (whole) {
+          const uint32_t dst = box_addr(k) + lane * 128;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[32 + e] = w[e];
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(dst + ((u ^ (lane & 7)) << 4),
+                         __float_as_uint(__uint_as_float(v[4 * u]) * a.scale),
+                         __float_as_uint(__uint_as_float(v[4 * u + 1]) * a.scale),
+                         __float_as_uint(__uint_as_float(v[4 * u + 2]) * a.scale),
+                         __float_as_uint(__uint_as_float(v[4 * u + 3]) * a.scale));
+        } else if (q_ok) {
+          dq_row_out(row + k * 32, v, a.scale, packed);
+        }
       }
-      if constexpr (D == 128) {
-        if (q_ok) dq_out<D>(row, v, a.scale, packed);
-        uint32_t w[32];
-        tmem_ld_x32(tl + C::kColDP + 64, w);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.dq_empty));  // dQ TMEM columns free for the next dP
+      if (whole) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (whole) {
+          const int y = static_cast<int>(q_base + int64_t(m) * 128 + wq * 32);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = w[e];
-        tmem_ld_x32(tl + C::kColDP + 96, w);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[32 + e] = w[e];
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.dq_empty));  // TMEM released before the last reductions
-        if (q_ok) dq_out<D>(row + 64, v, a.scale, packed);
-      } else {
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.dq_empty));
-        if (q_ok) dq_out<D>(row, v, a.scale, packed);
+          for (int k = 0; k < D / 32; ++k) {
+            if (packed) tma_store_2d(dq_map, box_addr(k), t.h * D + k * 32, y);
+            else tma_reduce_add_2d(dq_map, box_addr(k), t.h * D + k * 32, y);
+          }
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(smem_u32(&bars.q_empty[qs]));
       }
+      __syncwarp();
     }
   }
 }
@@ -508,7 +530,7 @@ template <int D, bool kPack>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     jfa_bwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap do_map,
-                   const BwdArgs a) {
+                   const __grid_constant__ CUtensorMap dq_map, const BwdArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -524,7 +546,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.q_full[s]), 1);
-      mbar_init(smem_u32(&bars.q_empty[s]), 1);
+      mbar_init(smem_u32(&bars.q_empty[s]), 4);  // one arrival per drain warp
     }
     mbar_init(smem_u32(&bars.s_full), 1);
     mbar_init(smem_u32(&bars.dp_full), 1);
@@ -556,7 +578,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   if (warp < 8) {
     bwd_softmax<D, kPack>(a, smem, sbase, tmem, bars, ab, t_begin, t_end, warp >> 2);
   } else if (warp >= C::kDrainWarp0) {
-    bwd_drain<D, kPack>(a, tmem, bars, ab, t_begin, t_end);
+    bwd_drain<D, kPack>(a, &dq_map, sbase, tmem, bars, ab, t_begin, t_end);
+    if (lane == 0) bulk_wait_all();  // dQ boxes written before the CTA exits
   } else if (warp == C::kProducerWarp) {
     if (lane == 0) bwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, t_begin, t_end);
     __syncwarp();
@@ -574,7 +597,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
 template <int D, bool kPack>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
-                         const CUtensorMap& v, const CUtensorMap& dO, int grid, cudaStream_t stream) {
+                         const CUtensorMap& v, const CUtensorMap& dO, const CUtensorMap& dq,
+                         int grid, cudaStream_t stream) {
   using C = BwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static bool configured = false;
@@ -584,7 +608,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorM
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  jfa_bwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, a);
+  jfa_bwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, dq, a);
   return cudaGetLastError();
 }
 
@@ -604,13 +628,13 @@ cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta
 
 namespace jfa {
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
-                       const CUtensorMap& v_map, const CUtensorMap& do_map, int grid,
-                       cudaStream_t stream) {
+                       const CUtensorMap& v_map, const CUtensorMap& do_map,
+                       const CUtensorMap& dq_map, int grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   if (a.pb.D == 128)
-    return a.packed ? launch_bwd_d<128, true>(a, q_map, k_map, v_map, do_map, grid, stream)
-                    : launch_bwd_d<128, false>(a, q_map, k_map, v_map, do_map, grid, stream);
-  return a.packed ? launch_bwd_d<64, true>(a, q_map, k_map, v_map, do_map, grid, stream)
-                  : launch_bwd_d<64, false>(a, q_map, k_map, v_map, do_map, grid, stream);
+    return a.packed ? launch_bwd_d<128, true>(a, q_map, k_map, v_map, do_map, dq_map, grid, stream)
+                    : launch_bwd_d<128, false>(a, q_map, k_map, v_map, do_map, dq_map, grid, stream);
+  return a.packed ? launch_bwd_d<64, true>(a, q_map, k_map, v_map, do_map, dq_map, grid, stream)
+                  : launch_bwd_d<64, false>(a, q_map, k_map, v_map, do_map, dq_map, grid, stream);
 }
 }  // namespace jfa

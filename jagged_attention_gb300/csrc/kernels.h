@@ -50,9 +50,10 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtenso
 cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta, int64_t n_o,
                          int H, int D, cudaStream_t stream);
 
-// Backward main pass (grid = P CTAs).
+// Backward main pass (grid = P CTAs).  dq_map: fp32 dQ as [rows, H*D] in
+// boxes of 32 x 32 with the 128-byte swizzle.
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
-                       const CUtensorMap& v_map, const CUtensorMap& do_map, int grid,
-                       cudaStream_t stream);
+                       const CUtensorMap& v_map, const CUtensorMap& do_map,
+                       const CUtensorMap& dq_map, int grid, cudaStream_t stream);
 
 }  // namespace jfa
