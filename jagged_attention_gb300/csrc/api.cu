@@ -38,14 +38,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 128 rows x 64 columns (128 bytes) with the 128-byte swizzle the MMA
 // descriptors expect.  Rows past the end read as zeros.  An empty tensor gets
 // a zeroed descriptor that no tile ever uses.
-int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+// box_rows = 32: the unit one warp of the backward stores dK or dV in.
+int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, unsigned box_rows = 128) {
   std::memset(m, 0, sizeof(*m));
   if (rows == 0) return JFA_OK;
   auto enc = tensor_map_encoder();
   if (!enc) return JFA_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -361,10 +362,11 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
     return JFA_ERR_WORKSPACE;
   if (plan->bwd.P == 0) return JFA_OK;
   const int64_t cols = int64_t(plan->H) * plan->D;
-  CUtensorMap qm, km, vm, dom, dqm;
+  CUtensorMap qm, km, vm, dom, dqm, dkm, dvm;
   if (make_map(&qm, q, plan->n_q, cols) || make_map(&km, k, plan->n_kv, cols) ||
       make_map(&vm, v, plan->n_kv, cols) || make_map(&dom, dout, plan->n_o, cols) ||
-      make_map_dq(&dqm, dq, plan->n_q, cols))
+      make_map_dq(&dqm, dq, plan->n_q, cols) || make_map(&dkm, dk, plan->n_kv, cols, 32) ||
+      make_map(&dvm, dv, plan->n_kv, cols, 32))
     return JFA_ERR_CUDA;
   jfa::BwdArgs a;
   a.pb = problem_of(plan);
@@ -380,7 +382,7 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
   a.status = plan->d_status;
   a.packed = plan->packed;
   cudaError_t e =
-      jfa::launch_bwd(a, qm, km, vm, dom, dqm, plan->bwd.P, static_cast<cudaStream_t>(stream));
+      jfa::launch_bwd(a, qm, km, vm, dom, dqm, dkm, dvm, plan->bwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
@@ -499,9 +501,10 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   cudaError_t e = jfa::launch_delta(static_cast<const uint16_t*>(out),
                                     static_cast<const uint16_t*>(dout), delta, n_o, H, D, s);
   if (e != cudaSuccess) return JFA_ERR_CUDA;
-  CUtensorMap qm, km, vm, dom, dqm;
+  CUtensorMap qm, km, vm, dom, dqm, dkm, dvm;
   if (make_map(&qm, q, n_q, cols) || make_map(&km, k, n_kv, cols) || make_map(&vm, v, n_kv, cols) ||
-      make_map(&dom, dout, n_o, cols) || make_map_dq(&dqm, dq, n_q, cols))
+      make_map(&dom, dout, n_o, cols) || make_map_dq(&dqm, dq, n_q, cols) ||
+      make_map(&dkm, dk, n_kv, cols, 32) || make_map(&dvm, dv, n_kv, cols, 32))
     return JFA_ERR_CUDA;
   jfa::BwdArgs a;
   a.pb.kv_off = reinterpret_cast<const int32_t*>(scratch + o_kv);
@@ -524,7 +527,7 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   a.dv = static_cast<uint16_t*>(dv);
   a.status = device_status ? device_status : reinterpret_cast<int*>(scratch + o_st);
   a.packed = false;
-  e = jfa::launch_bwd(a, qm, km, vm, dom, dqm, sched.P, s);
+  e = jfa::launch_bwd(a, qm, km, vm, dom, dqm, dkm, dvm, sched.P, s);
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

@@ -399,35 +399,73 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
 // here, in the memory system).  At the end of a tile the group writes dV and
 // scale * dK (thread = key row) before the tile's last dQ, so the next tile's
 // products do not wait for them.
+// dV and scale * dK of the tile (thread = key row), bf16.  A warp whose 32 key
+// rows all belong to the tile writes them into shared memory in the
+// 128-byte-swizzled box layout (dV in the Q stage, dK in the dO stage of the
+// step just finished, 64-column chunks 16 KB apart) and stores them as D/64
+// boxes of 32 x 64 each; a warp with rows past the sequence stores its valid
+// rows directly.  Returns whether this warp staged (its lane 0 then owns an
+// open bulk group reading the stage).
 template <int D, bool kPack>
-__device__ __forceinline__ void dkv_epilogue(const BwdArgs& a, uint32_t tl, const BTile& t, int r) {
+__device__ __forceinline__ bool dkv_epilogue(const BwdArgs& a, const CUtensorMap* dk_map,
+                                             const CUtensorMap* dv_map, uint32_t sbase, uint32_t qs,
+                                             uint32_t tl, const BTile& t, int wq, int lane,
+                                             uint32_t dkv_empty) {
   using C = BwdCfg<D>;
   const int H = a.pb.H;
+  const int r = wq * 32 + lane;
   const bool packed = kPack && t.n < 0;  // packed tile: rows of -n short sequences
   const int nb = packed ? 0 : t.n;
   const int64_t klen = a.pb.kv_off[t.b + (packed ? -t.n : 1)] - a.pb.kv_off[t.b];
   const bool kv_ok = int64_t(nb) * 128 + r < klen;
+  const bool whole = __all_sync(0xffffffffu, kv_ok);
   const int64_t krow = int64_t(a.pb.kv_off[t.b]) + nb * 128 + r;
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
     const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
     const float mul = which == 0 ? 1.0f : a.scale;
     uint16_t* dst_row = (which == 0 ? a.dv : a.dk) + (krow * H + t.h) * D;
+    const uint32_t stage = sbase + (which == 0 ? C::kOffQ : C::kOffDO) + qs * C::kTileBytes + wq * 4096 +
+                           lane * 128;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t w[32];
       tmem_ld_x32(tl + col + c * 32, w);
-      if (kv_ok) {
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(w[2 * e]) * mul, __uint_as_float(w[2 * e + 1]) * mul);
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack_bf16x2(__uint_as_float(w[2 * e]) * mul, __uint_as_float(w[2 * e + 1]) * mul);
+      if (whole) {
+        // 32 columns = units 4(c&1) .. 4(c&1)+3 of the row in chunk c/2
+        const uint32_t dst = stage + (c >> 1) * 16384;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(dst + (((4 * (c & 1) + q) ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                       pk[4 * q + 2], pk[4 * q + 3]);
+      } else if (kv_ok) {
         uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
 #pragma unroll
         for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
     }
   }
+  tc_fence_before();
+  mbar_arrive(dkv_empty);  // dK / dV TMEM columns free for the next tile
+  if (whole) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const int y = static_cast<int>(int64_t(a.pb.kv_off[t.b]) + nb * 128 + wq * 32);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const uint32_t off = qs * C::kTileBytes + wq * 4096 + c * 16384;
+        tma_store_2d(dv_map, sbase + C::kOffQ + off, t.h * D + c * 64, y);
+        tma_store_2d(dk_map, sbase + C::kOffDO + off, t.h * D + c * 64, y);
+      }
+      bulk_commit();
+    }
+  }
+  return whole;
 }
 
 // 32 dQ columns of one row: reduce-added, or stored when this tile owns the row.
@@ -452,8 +490,9 @@ __device__ __forceinline__ void dq_row_out(float* row, const uint32_t (&v)[32], 
 // returns to the producer when every drain warp's boxes have been read out.
 // A warp whose rows run past the sequence writes its valid rows directly.
 template <int D, bool kPack>
-__device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, uint32_t sbase,
-                          uint32_t tmem, BwdBars& bars, const Abort& ab, int t_begin, int t_end) {
+__device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUtensorMap* dk_map,
+                          const CUtensorMap* dv_map, uint32_t sbase, uint32_t tmem, BwdBars& bars,
+                          const Abort& ab, int t_begin, int t_end) {
   using C = BwdCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
@@ -468,17 +507,19 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, uint32_t 
     const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + (packed ? -t.n : 1)] - a.pb.q_off[t.b]) : a.pb.Lq;
     const int64_t q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
     for (int m = 0; m < t.qblocks; ++m, ++gm) {
+      const uint32_t qs = gm & 1;
       if (m == t.qblocks - 1) {
+        // dkv_full fires with this step's dq_full: the Q/dO stage is free
         if (!warp_wait_b(smem_u32(&bars.dkv_full), tt & 1, ab)) return;
         tc_fence_after();
-        dkv_epilogue<D, kPack>(a, tl, t, r);
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.dkv_empty));
+        const bool staged = dkv_epilogue<D, kPack>(a, dk_map, dv_map, sbase, qs, tl, t, wq, lane,
+                                                   smem_u32(&bars.dkv_empty));
+        if (staged && lane == 0) bulk_wait_read_all();  // the stage is reused for dQ below
+        __syncwarp();
         ++tt;
       }
       if (!warp_wait_b(smem_u32(&bars.dq_full), gm & 1, ab)) return;
       tc_fence_after();
-      const uint32_t qs = gm & 1;
       const bool q_ok = int64_t(m) * 128 + r < qlen;
       const bool whole = __all_sync(0xffffffffu, q_ok);
       float* row = a.dq + ((q_base + int64_t(m) * 128 + r) * H + t.h) * D;
@@ -530,7 +571,8 @@ template <int D, bool kPack>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     jfa_bwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap do_map,
-                   const __grid_constant__ CUtensorMap dq_map, const BwdArgs a) {
+                   const __grid_constant__ CUtensorMap dq_map, const __grid_constant__ CUtensorMap dk_map,
+                   const __grid_constant__ CUtensorMap dv_map, const BwdArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -578,8 +620,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   if (warp < 8) {
     bwd_softmax<D, kPack>(a, smem, sbase, tmem, bars, ab, t_begin, t_end, warp >> 2);
   } else if (warp >= C::kDrainWarp0) {
-    bwd_drain<D, kPack>(a, &dq_map, sbase, tmem, bars, ab, t_begin, t_end);
-    if (lane == 0) bulk_wait_all();  // dQ boxes written before the CTA exits
+    bwd_drain<D, kPack>(a, &dq_map, &dk_map, &dv_map, sbase, tmem, bars, ab, t_begin, t_end);
+    if (lane == 0) bulk_wait_all();  // dQ, dK, dV boxes written before the CTA exits
   } else if (warp == C::kProducerWarp) {
     if (lane == 0) bwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, t_begin, t_end);
     __syncwarp();
@@ -598,7 +640,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 template <int D, bool kPack>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, const CUtensorMap& dO, const CUtensorMap& dq,
-                         int grid, cudaStream_t stream) {
+                         const CUtensorMap& dk, const CUtensorMap& dv, int grid, cudaStream_t stream) {
   using C = BwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static bool configured = false;
@@ -608,7 +650,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorM
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  jfa_bwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, dq, a);
+  jfa_bwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, dq, dk, dv, a);
   return cudaGetLastError();
 }
 
@@ -629,12 +671,13 @@ cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta
 namespace jfa {
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
                        const CUtensorMap& v_map, const CUtensorMap& do_map,
-                       const CUtensorMap& dq_map, int grid, cudaStream_t stream) {
+                       const CUtensorMap& dq_map, const CUtensorMap& dk_map,
+                       const CUtensorMap& dv_map, int grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
+#define JFA_BWD_ARGS a, q_map, k_map, v_map, do_map, dq_map, dk_map, dv_map, grid, stream
   if (a.pb.D == 128)
-    return a.packed ? launch_bwd_d<128, true>(a, q_map, k_map, v_map, do_map, dq_map, grid, stream)
-                    : launch_bwd_d<128, false>(a, q_map, k_map, v_map, do_map, dq_map, grid, stream);
-  return a.packed ? launch_bwd_d<64, true>(a, q_map, k_map, v_map, do_map, dq_map, grid, stream)
-                  : launch_bwd_d<64, false>(a, q_map, k_map, v_map, do_map, dq_map, grid, stream);
+    return a.packed ? launch_bwd_d<128, true>(JFA_BWD_ARGS) : launch_bwd_d<128, false>(JFA_BWD_ARGS);
+  return a.packed ? launch_bwd_d<64, true>(JFA_BWD_ARGS) : launch_bwd_d<64, false>(JFA_BWD_ARGS);
+#undef JFA_BWD_ARGS
 }
 }  // namespace jfa

@@ -50,10 +50,12 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtenso
 cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta, int64_t n_o,
                          int H, int D, cudaStream_t stream);
 
-// Backward main pass (grid = P CTAs).  dq_map: fp32 dQ as [rows, H*D] in
-// boxes of 32 x 32 with the 128-byte swizzle.
+// Backward main pass (grid = P CTAs).  Output maps, [rows, H*D] with the
+// 128-byte swizzle: dq_map fp32 in boxes of 32 x 32, dk_map / dv_map bf16 in
+// boxes of 32 rows x 64 columns.
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
                        const CUtensorMap& v_map, const CUtensorMap& do_map,
-                       const CUtensorMap& dq_map, int grid, cudaStream_t stream);
+                       const CUtensorMap& dq_map, const CUtensorMap& dk_map,
+                       const CUtensorMap& dv_map, int grid, cudaStream_t stream);
 
 }  // namespace jfa
