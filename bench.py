@@ -69,7 +69,45 @@ def flops(prob, which: str) -> float:
     return base if which == "fwd" else 2.5 * base
 
 
-def alg_bytes(prob, which: str) -> float:
+def dq_rows_cleared(prob, pack: bool) -> int:
+    """Query rows whose fp32 dQ the backward pre-pass clears: the library clears
+    the rows tiles reduce-add into or never write (all rows in broadcast mode;
+    otherwise sequences with no key or more than one 128-key block, unless
+    packed), and clears everything when that leaves more than four runs or
+    more than half of the rows."""
+    if prob.mode == "broadcast":
+        return prob.n_q_rows
+    klen, qlen = prob.kv_lengths, prob.q_lengths
+    packed = np.zeros(len(klen), dtype=bool)
+    if pack:  # greedy runs of short sequences totalling <= 128 rows, >= 2 non-empty
+        b = 0
+        while b < len(klen):
+            if klen[b] == 0 or klen[b] > 128:
+                b += 1
+                continue
+            total, e, nonempty = klen[b], b + 1, 1
+            while e < len(klen) and total + klen[e] <= 128:
+                total += klen[e]
+                nonempty += klen[e] > 0
+                e += 1
+            if nonempty >= 2:
+                packed[b:e] = True
+                b = e
+            else:
+                b += 1
+    runs, rows, prev_end, pos = 0, 0, -1, 0
+    for b in range(len(qlen)):
+        s, e = pos, pos + int(qlen[b])
+        pos = e
+        if e == s or packed[b] or 0 < klen[b] <= 128:
+            continue
+        runs += 0 if s == prev_end else 1
+        rows += e - s
+        prev_end = e
+    return prob.n_q_rows if (runs > 4 or 2 * rows > prob.n_q_rows) else rows
+
+
+def alg_bytes(prob, which: str, pack: bool = False) -> float:
     """Algorithmic HBM bytes of one launch (each tensor read or written once)."""
     row = prob.H * prob.D
     q = prob.n_q_rows * row * 2
@@ -78,8 +116,8 @@ def alg_bytes(prob, which: str) -> float:
     lse = prob.n_o_rows * prob.H * 4
     if which == "fwd":
         return q + 2 * kv + o + lse
-    if which == "pre":  # O and dO read, Delta written, dQ cleared
-        return 2 * o + lse + prob.n_q_rows * row * 4
+    if which == "pre":  # O and dO read, Delta written, the reduce-added dQ rows cleared
+        return 2 * o + lse + dq_rows_cleared(prob, pack) * row * 4
     # main: Q, K, V, dO, LSE, Delta read; dQ (fp32), dK, dV written
     return q + 2 * kv + o + 2 * lse + prob.n_q_rows * row * 4 + 2 * kv
 
@@ -308,7 +346,7 @@ def run_ours(args, rank, world, dist):
     per_kernel = {
         "jfa_fwd_kernel": {"ms": k_fwd / args.steps, "flops": flops(prob, "fwd"),
                            "bytes": alg_bytes(prob, "fwd"), "src": "fwd.cu"},
-        "bwd_preprocess": {"ms": k_pre / args.steps, "flops": 0.0, "bytes": alg_bytes(prob, "pre"),
+        "bwd_preprocess": {"ms": k_pre / args.steps, "flops": 0.0, "bytes": alg_bytes(prob, "pre", args.pack),
                            "src": "bwd.cu"},
         "jfa_bwd_kernel": {"ms": k_main / args.steps, "flops": flops(prob, "bwd"),
                            "bytes": alg_bytes(prob, "main"), "src": "bwd.cu"},

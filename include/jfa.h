@@ -157,11 +157,14 @@ int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const 
 /*
  * The two stages jfa_bwd runs, for callers that schedule them separately
  * (same arguments and rules as jfa_bwd).
- * jfa_bwd_preprocess: Delta (into workspace) from out and dout, clears dq
- *   (unless every sequence sits in a packed tile, whose dQ rows are stored
- *   outright), and zeroes dk / dv rows of sequences with keys but no queries.
+ * jfa_bwd_preprocess: Delta (into workspace) from out and dout, clears the dq
+ *   rows the main pass reduce-adds into or never writes (all of them in
+ *   broadcast mode; with query offsets, those of sequences with no key or
+ *   more than one key block -- a sequence with one key block, or in a packed
+ *   tile, has its dQ rows stored outright by its one tile), and zeroes dk / dv
+ *   rows of sequences with keys but no queries.
  * jfa_bwd_main: the key/value-stationary pass; needs the workspace written by
- *   jfa_bwd_preprocess (stream order) and the cleared dq.
+ *   jfa_bwd_preprocess (stream order) and the dq rows it cleared.
  */
 int jfa_bwd_preprocess(jfa_plan_t plan, const void* out, const void* dout, float* dq, void* dk,
                        void* dv, void* workspace, size_t workspace_bytes, void* stream);
@@ -210,6 +213,20 @@ int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
                     int Lq, int D, const void* q, const void* k, const void* v, const void* out,
                     const void* dout, const float* lse, float scale, float* dq, void* dk, void* dv,
                     int* device_status, void* stream);
+
+/*
+ * Self-test of the failure path (no counterpart in the pages; it exists so
+ * the timeout handling every kernel relies on can be exercised on a GPU
+ * without a fault).  Launches one CTA whose waiting thread runs the kernels'
+ * bounded mbarrier wait on a barrier nothing arrives on, with the limit
+ * shortened to limit_us microseconds (1 .. 2,000,000), and synchronises the
+ * stream.  Expected result: JFA_ERR_DEVICE_TIMEOUT, with the wait's measured
+ * duration in *waited_ns (may be NULL); the kernel returns normally, so the
+ * context stays usable.  JFA_OK would mean the wait completed (it cannot);
+ * JFA_ERR_CUDA reports a failed launch.  The status word is one static device
+ * variable: calls on different streams race.
+ */
+int jfa_selftest_wait_timeout(unsigned limit_us, unsigned long long* waited_ns, void* stream);
 
 /* Human-readable text of a status code (static storage). */
 const char* jfa_status_string(int status);

@@ -87,6 +87,19 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> tuple[int, int]:
+    """Run the library's bounded-wait self-test (jfa_selftest_wait_timeout):
+    returns (status code, measured wait in ns).  JFA_ERR_DEVICE_TIMEOUT (7) is
+    the expected status."""
+    L = lib()
+    fn = L.jfa_selftest_wait_timeout
+    fn.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_ulonglong), _vp]
+    fn.restype = ctypes.c_int
+    waited = ctypes.c_ulonglong()
+    rc = fn(int(limit_us), ctypes.byref(waited), None if not torch.cuda.is_available() else _stream(stream))
+    return rc, waited.value
+
+
 def _check(rc: int, where: str):
     if rc != JFA_OK:
         raise JfaError(rc, where)

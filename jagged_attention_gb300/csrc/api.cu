@@ -192,11 +192,30 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   p->n_kv = n_kv;
   std::vector<int> pack;
   p->packed = use_packing(flags, kv_offsets_host, q_offsets_host, B);
-  if (p->packed) {
-    pack = jfa::short_packs(kvlen);
-    p->all_packed = true;
-    for (int b = 0; b < B; ++b)
-      if (kvlen[b] > 0 && pack[b] == 1) p->all_packed = false;
+  if (p->packed) pack = jfa::short_packs(kvlen);
+  if (!q_offsets_host) {
+    if (n_q > 0) p->dq_rows_to_clear.emplace_back(0, n_q);
+  } else {
+    for (int b = 0; b < B; ++b) {
+      const int64_t s = q_offsets_host[b], e = q_offsets_host[b + 1];
+      if (e == s) continue;
+      if (p->packed && pack[b] != 1) continue;   // a packed tile stores these rows
+      if (kvlen[b] > 0 && kvlen[b] <= jfa::kBN) continue;  // one key block: its tile stores
+      if (!p->dq_rows_to_clear.empty() && p->dq_rows_to_clear.back().second == s)
+        p->dq_rows_to_clear.back().second = e;
+      else
+        p->dq_rows_to_clear.emplace_back(s, e);
+    }
+    // many runs, or most of the rows: one clear of the whole dQ costs less
+    // than a launch per run (clearing rows a tile then stores is harmless)
+    int64_t rows = 0;
+    for (const auto& r : p->dq_rows_to_clear) rows += r.second - r.first;
+    if (p->dq_rows_to_clear.size() > 4 || 2 * rows > n_q) {
+      p->dq_rows_to_clear.clear();
+      p->dq_rows_to_clear.emplace_back(0, n_q);
+    } else {
+      p->dq_own_rows = true;
+    }
   }
   p->fwd = jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr);
   p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr);
@@ -328,11 +347,14 @@ int jfa_bwd_preprocess(jfa_plan_t plan, const void* out, const void* dout, float
     return JFA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t cols = int64_t(plan->H) * plan->D;
-  // dQ is reduce-added by the key/value tiles: start from zero (packed tiles
-  // store their rows, so a fully packed plan needs no clearing)
-  if (plan->n_q > 0 && !plan->all_packed &&
-      cudaMemsetAsync(dq, 0, static_cast<size_t>(plan->n_q) * cols * sizeof(float), s) != cudaSuccess)
-    return JFA_ERR_CUDA;
+  // dQ rows that tiles reduce-add into (or that no tile touches) start from
+  // zero; rows a single tile owns are stored by it
+  for (const auto& run : plan->dq_rows_to_clear) {
+    const size_t off = static_cast<size_t>(run.first) * cols * sizeof(float);
+    const size_t len = static_cast<size_t>(run.second - run.first) * cols * sizeof(float);
+    if (cudaMemsetAsync(reinterpret_cast<uint8_t*>(dq) + off, 0, len, s) != cudaSuccess)
+      return JFA_ERR_CUDA;
+  }
   // keys of sequences without queries get no backward tile: their gradients are zero
   for (const auto& run : plan->kv_rows_without_queries) {
     const size_t off = static_cast<size_t>(run.first) * cols * 2;
@@ -381,6 +403,7 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
   a.dv = static_cast<uint16_t*>(dv);
   a.status = plan->d_status;
   a.packed = plan->packed;
+  a.own_rows = plan->dq_own_rows;
   cudaError_t e =
       jfa::launch_bwd(a, qm, km, vm, dom, dqm, dkm, dvm, plan->bwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;

@@ -484,12 +484,13 @@ __device__ __forceinline__ void dq_row_out(float* row, const uint32_t (&v)[32], 
 // scattered 16-byte pieces at a fraction of the rate of whole rows.  So each
 // drain warp writes its 32 rows into shared memory in the 128-byte-swizzled
 // box layout and hands them to the tensor-memory-access unit as D/32 boxes of
-// 32 x 32 fp32 (reduce-add, or store for packed tiles).  The staging space is
+// 32 x 32 fp32 (reduce-add, or store when the tile owns the rows).  The staging space is
 // the Q/dO stage of the step just finished, free once dq_full has fired: its
 // D/32 boxes of 16 KB fill the Q stage first, then the dO stage.  The stage
 // returns to the producer when every drain warp's boxes have been read out.
 // A warp whose rows run past the sequence writes its valid rows directly.
-template <int D, bool kPack>
+// kSelf: queries have their own offsets, so a tile can own its dQ rows.
+template <int D, bool kPack, bool kSelf>
 __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUtensorMap* dk_map,
                           const CUtensorMap* dv_map, uint32_t sbase, uint32_t tmem, BwdBars& bars,
                           const Abort& ab, int t_begin, int t_end) {
@@ -502,8 +503,11 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
   uint32_t gm = 0, tt = 0;
   for (int i = t_begin; i < t_end; ++i) {
     const BTile t = load_btile(a.tiles, i);
-    // a packed tile is the only one touching its sequences' dQ rows: store
+    // a tile that is the only one touching its dQ rows stores them instead of
+    // reduce-adding: a packed tile, or (queries with their own offsets) the one
+    // tile of a sequence with a single key block
     const bool packed = kPack && t.n < 0;
+    const bool store = packed || (kSelf && a.pb.kv_off[t.b + 1] - a.pb.kv_off[t.b] <= 128);
     const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + (packed ? -t.n : 1)] - a.pb.q_off[t.b]) : a.pb.Lq;
     const int64_t q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
     for (int m = 0; m < t.qblocks; ++m, ++gm) {
@@ -542,7 +546,7 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
                          __float_as_uint(__uint_as_float(v[4 * u + 2]) * a.scale),
                          __float_as_uint(__uint_as_float(v[4 * u + 3]) * a.scale));
         } else if (q_ok) {
-          dq_row_out(row + k * 32, v, a.scale, packed);
+          dq_row_out(row + k * 32, v, a.scale, store);
         }
       }
       tc_fence_before();
@@ -554,7 +558,7 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
           const int y = static_cast<int>(q_base + int64_t(m) * 128 + wq * 32);
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) {
-            if (packed) tma_store_2d(dq_map, box_addr(k), t.h * D + k * 32, y);
+            if (store) tma_store_2d(dq_map, box_addr(k), t.h * D + k * 32, y);
             else tma_reduce_add_2d(dq_map, box_addr(k), t.h * D + k * 32, y);
           }
           bulk_commit();
@@ -567,7 +571,7 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
   }
 }
 
-template <int D, bool kPack>
+template <int D, bool kPack, bool kSelf>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     jfa_bwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap do_map,
@@ -620,7 +624,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   if (warp < 8) {
     bwd_softmax<D, kPack>(a, smem, sbase, tmem, bars, ab, t_begin, t_end, warp >> 2);
   } else if (warp >= C::kDrainWarp0) {
-    bwd_drain<D, kPack>(a, &dq_map, &dk_map, &dv_map, sbase, tmem, bars, ab, t_begin, t_end);
+    bwd_drain<D, kPack, kSelf>(a, &dq_map, &dk_map, &dv_map, sbase, tmem, bars, ab, t_begin, t_end);
     if (lane == 0) bulk_wait_all();  // dQ, dK, dV boxes written before the CTA exits
   } else if (warp == C::kProducerWarp) {
     if (lane == 0) bwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, t_begin, t_end);
@@ -637,7 +641,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool kPack>
+template <int D, bool kPack, bool kSelf>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, const CUtensorMap& dO, const CUtensorMap& dq,
                          const CUtensorMap& dk, const CUtensorMap& dv, int grid, cudaStream_t stream) {
@@ -645,12 +649,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorM
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(jfa_bwd_kernel<D, kPack>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(jfa_bwd_kernel<D, kPack, kSelf>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  jfa_bwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, dq, dk, dv, a);
+  jfa_bwd_kernel<D, kPack, kSelf><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, dq, dk, dv, a);
   return cudaGetLastError();
 }
 
@@ -675,9 +679,16 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtenso
                        const CUtensorMap& dv_map, int grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
 #define JFA_BWD_ARGS a, q_map, k_map, v_map, do_map, dq_map, dk_map, dv_map, grid, stream
+  // packed plans, plans whose single-key-block tiles store their dQ rows, and
+  // plans where every tile reduce-adds run separate instantiations
+  const bool self = a.own_rows;
   if (a.pb.D == 128)
-    return a.packed ? launch_bwd_d<128, true>(JFA_BWD_ARGS) : launch_bwd_d<128, false>(JFA_BWD_ARGS);
-  return a.packed ? launch_bwd_d<64, true>(JFA_BWD_ARGS) : launch_bwd_d<64, false>(JFA_BWD_ARGS);
+    return a.packed ? launch_bwd_d<128, true, true>(JFA_BWD_ARGS)
+                    : self ? launch_bwd_d<128, false, true>(JFA_BWD_ARGS)
+                           : launch_bwd_d<128, false, false>(JFA_BWD_ARGS);
+  return a.packed ? launch_bwd_d<64, true, true>(JFA_BWD_ARGS)
+                  : self ? launch_bwd_d<64, false, true>(JFA_BWD_ARGS)
+                         : launch_bwd_d<64, false, false>(JFA_BWD_ARGS);
 #undef JFA_BWD_ARGS
 }
 }  // namespace jfa

@@ -40,6 +40,8 @@ struct BwdArgs {
   uint16_t* dv;
   int* status;
   bool packed;             // the schedule may hold packed tiles {b0, h, -nseq, 1}
+  bool own_rows = false;   // the pre-pass left the dQ rows of single-key-block
+                           // sequences uncleared: their one tile stores them
 };
 
 // Forward: one persistent launch over the schedule (grid = P CTAs).

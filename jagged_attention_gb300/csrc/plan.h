@@ -46,7 +46,13 @@ struct jfa_plan {
   int B = 0, H = 0, Lq = 0, D = 0;
   bool broadcast = false;
   bool packed = false;       // short sequences packed into shared tiles
-  bool all_packed = false;   // every sequence with rows sits in a packed tile
+  // query row ranges [begin, end) whose dQ the backward reduce-adds (or never
+  // writes) and the pre-pass therefore clears: broadcast mode's shared rows,
+  // and in self mode the sequences with no key or more than one key block
+  // (a sequence with one key block, or in a packed tile, has one tile that
+  // stores its rows)
+  std::vector<std::pair<int64_t, int64_t>> dq_rows_to_clear;
+  bool dq_own_rows = false;  // some rows are left to the tiles that own them
   int device = 0;
   int num_ctas = 0;
   int64_t n_q = 0;   // rows of Q

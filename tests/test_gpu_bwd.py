@@ -90,3 +90,20 @@ def test_packed_short_sequences(D):
 def test_packed_block_diagonal_segments():
     import jagged_attention_gb300 as jfa
     _run(workloads.make_problem(24, 2, 128, "self", [64] * 24, seed=21), flags=jfa.PLAN_PACK_SHORT)
+
+
+# Mostly short sequences plus two long ones: the pre-pass clears only the long
+# ones' dQ rows and the tiles of single-key-block sequences store theirs
+# (dQ is NaN-prefilled, so a row neither cleared nor stored would show up).
+OWNER_LENGTHS = [50, 128, 1, 300, 64, 64, 100, 90, 20, 129, 77]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_single_key_block_sequences_store_their_dq(D):
+    _run(workloads.make_problem(len(OWNER_LENGTHS), 2, D, "self", OWNER_LENGTHS, seed=22))
+
+
+def test_single_key_block_cross_attention():
+    # queries with their own offsets: one key block but several query blocks
+    _run(workloads.make_problem(4, 2, 128, "self", [100, 128, 700, 40],
+                                q_lengths=[300, 0, 129, 257], seed=23))

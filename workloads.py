@@ -12,6 +12,10 @@ Recipes (all seeded; seed 0 is the timing seed, seeds 0-2 the parity seeds):
     - ``skewed(frac, short, long)`` -> ``B - round(frac * B)`` short lengths drawn
       first, then ``round(frac * B)`` long lengths, concatenated and shuffled
     - ``fixed(L)`` -> every length equal to ``L``
+    - ``sparsity(s, Lmax)`` -> lengths whose mean is ``(1 - s) * Lmax``, so that
+      a fraction ``s`` of the padded [B, Lmax] grid is empty: uniform
+      ``[round((1 - 2s) Lmax), Lmax]`` for ``s <= 0.5``, uniform
+      ``[1, round(2 (1 - s) Lmax)]`` above
 * tensors are N(0, 1) fp32 draws from a ``torch.Generator`` seeded with ``seed``
   on the device the tensor lives on, in the order q, k, v, dout, then rounded
   to bf16 (round to nearest even).  CPU and CUDA generators give different
@@ -19,10 +23,11 @@ Recipes (all seeded; seed 0 is the timing seed, seeds 0-2 the parity seeds):
   sides.
 * ``scale = 1 / sqrt(D)``.
 
-The five named workloads stand in for the production jagged shapes the JFA
-pages benchmark (GEM jagged / broadcast-Q shapes, the skewed-length load
-balancing case and the TLX Block Attention batch-1152, 4k-token, H=4, D=128
-block-diagonal case); the pages publish no dataset.
+The named workloads stand in for the production jagged shapes the JFA pages
+benchmark (GEM jagged / broadcast-Q shapes, the skewed-length load balancing
+case, the TLX Block Attention batch-1152, 4k-token, H=4, D=128
+block-diagonal case, the jagged broadcast-Q sparsity sweep 0.1 / 0.5 / 0.9
+and the dense B=768, H=4, D=128 case); the pages publish no dataset.
 """
 from __future__ import annotations
 
@@ -69,6 +74,25 @@ WORKLOADS = {
         lengths=("fixed", 64),
         note="block-diagonal self-attention: 1152 rows x 4096 tokens cut "
              "into 73,728 segments of 64, H=4 D=128"),
+    # jagged broadcast-Q sparsity sweep (measurement only)
+    "sparsity_0.1": Workload(
+        "sparsity_0.1", B=512, H=4, D=128, mode="broadcast", Lq=256,
+        lengths=("sparsity", 0.1, 2048),
+        note="broadcast-Q sweep point: B=512 H=4 D=128 Lq=256, 10% of a padded "
+             "[512, 2048] grid empty (lengths uniform [1638, 2048])"),
+    "sparsity_0.5": Workload(
+        "sparsity_0.5", B=512, H=4, D=128, mode="broadcast", Lq=256,
+        lengths=("sparsity", 0.5, 2048),
+        note="broadcast-Q sweep point: 50% empty (lengths uniform [0, 2048])"),
+    "sparsity_0.9": Workload(
+        "sparsity_0.9", B=512, H=4, D=128, mode="broadcast", Lq=256,
+        lengths=("sparsity", 0.9, 2048),
+        note="broadcast-Q sweep point: 90% empty (lengths uniform [1, 410])"),
+    "dense_768": Workload(
+        "dense_768", B=768, H=4, D=128, mode="self",
+        lengths=("fixed", 1024),
+        note="dense equal-length self-attention: B=768 H=4 D=128, every "
+             "sequence 1024 tokens (the pages give no length)"),
 }
 
 
@@ -91,6 +115,12 @@ def draw_lengths(recipe: tuple, B: int, seed: int) -> np.ndarray:
         rng.shuffle(out)
     elif kind == "fixed":
         out = np.full(B, recipe[1])
+    elif kind == "sparsity":
+        s, lmax = recipe[1], recipe[2]
+        if s <= 0.5:
+            out = rng.integers(int(round((1 - 2 * s) * lmax)), lmax + 1, size=B)
+        else:
+            out = rng.integers(1, int(round(2 * (1 - s) * lmax)) + 1, size=B)
     elif kind == "explicit":
         out = np.asarray(recipe[1])
         assert out.size == B
