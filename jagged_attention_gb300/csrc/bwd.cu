@@ -195,6 +195,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
   constexpr uint32_t id_kmaj = idesc_bf16_f32(128, D, false, true);    // dV (A in TMEM), dK
   constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);       // dQ: A = dS (M-major)
   const uint32_t sDS = sbase + C::kOffDS;
+  const uint64_t dsd_k = smem_desc_sw128(sDS, 16, 1024), dsd_m = smem_desc_sw128(sDS, C::kChunkBytes, 1024);
   uint32_t gm = 0, tt = 0;
   bool ok = true;
   for (int i = t_begin; i < t_end && ok; ++i) {
@@ -202,10 +203,16 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
     const uint32_t kb = tt & 1, vb = kb ^ 1;  // K and V buffers of this tile
     const uint32_t sK = sbase + C::kOffKV + kb * C::kTileBytes;
     const uint32_t sV = sbase + C::kOffKV + vb * C::kTileBytes;
+    const uint64_t kd_k = smem_desc_sw128(sK, 16, 1024), kd_m = smem_desc_sw128(sK, C::kChunkBytes, 1024);
+    const uint64_t vd_k = smem_desc_sw128(sV, 16, 1024);
     for (int m = 0; m < t.qblocks && ok; ++m, ++gm) {
       const uint32_t qs = gm & 1;
       const uint32_t sQ = sbase + C::kOffQ + qs * C::kTileBytes;
       const uint32_t sDO = sbase + C::kOffDO + qs * C::kTileBytes;
+      // operand descriptors of this step: K-major (16, 1024) and MN-major
+      // (chunk stride, 1024) views
+      const uint64_t qd_k = smem_desc_sw128(sQ, 16, 1024), qd_m = smem_desc_sw128(sQ, C::kChunkBytes, 1024);
+      const uint64_t dod_k = smem_desc_sw128(sDO, 16, 1024), dod_m = smem_desc_sw128(sDO, C::kChunkBytes, 1024);
       ok = mbar_wait(smem_u32(&bars.q_full[qs]), (gm >> 1) & 1, ab);
       if (ok && m == 0) ok = mbar_wait(smem_u32(&bars.kv_full[kb]), tt & 1, ab);
       // S^T region is free once the previous step's dV (which read P^T there) completed
@@ -215,8 +222,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-        mma_bf16_ss(tmem + C::kColS, smem_desc_sw128(sK + koff, 16, 1024),
-                    smem_desc_sw128(sQ + koff, 16, 1024), id_sdp, kk > 0 ? 1u : 0u);
+        mma_bf16_ss(tmem + C::kColS, desc_at(kd_k, koff), desc_at(qd_k, koff), id_sdp, kk > 0 ? 1u : 0u);
       }
       mma_commit(smem_u32(&bars.s_full));
       // dP^T region is free once WG1 has the previous dQ in registers
@@ -227,8 +233,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-        mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sV + koff, 16, 1024),
-                    smem_desc_sw128(sDO + koff, 16, 1024), id_sdp, kk > 0 ? 1u : 0u);
+        mma_bf16_ss(tmem + C::kColDP, desc_at(vd_k, koff), desc_at(dod_k, koff), id_sdp, kk > 0 ? 1u : 0u);
       }
       mma_commit(smem_u32(&bars.dp_full));
       if (m == t.qblocks - 1) mma_commit(smem_u32(&bars.kv_empty[vb]));  // V read for the last time
@@ -240,7 +245,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
       for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_m, K = 128 queries; P^T of query
                                        // half g sits at S columns [64g, 64g + 32)
         mma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                    smem_desc_sw128(sDO + kk * 2048, C::kChunkBytes, 1024), id_kmaj,
+                    desc_at(dod_m, kk * 2048), id_kmaj,
                     (m > 0 || kk > 0) ? 1u : 0u);
       mma_commit(smem_u32(&bars.dv_done));
       ok = mbar_wait(smem_u32(&bars.ds_full), gm & 1, ab);
@@ -249,13 +254,12 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_m
         mma_bf16_ss(tmem + C::kColDK,
-                    smem_desc_sw128(sDS + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32, 16, 1024),
-                    smem_desc_sw128(sQ + kk * 2048, C::kChunkBytes, 1024), id_kmaj,
+                    desc_at(dsd_k, (kk >> 2) * C::kChunkBytes + (kk & 3) * 32),
+                    desc_at(qd_m, kk * 2048), id_kmaj,
                     (m > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // dQ_m = dS K_n, K = 128 keys
-        mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sDS + kk * 2048, C::kChunkBytes, 1024),
-                    smem_desc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), id_dq,
+        mma_bf16_ss(tmem + C::kColDP, desc_at(dsd_m, kk * 2048), desc_at(kd_m, kk * 2048), id_dq,
                     kk > 0 ? 1u : 0u);
       mma_commit(smem_u32(&bars.dq_full));  // also: Q/dO stage qs read for the last time
       mma_commit(smem_u32(&bars.ds_empty));

@@ -170,7 +170,7 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
   using C = FwdCfg<D>;
   constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-  const uint32_t sQ = sbase + C::kOffQ;
+  const uint64_t qd = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
   uint32_t g = 0, tq = 0;
 
   // O += P_gp V_gp; `first` marks the first block of a tile (overwrite O).
@@ -180,13 +180,11 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
     if (!mbar_wait(smem_u32(&bars.p_full[pb]), (gp >> 1) & 1, ab)) return false;
     if (!mbar_wait(smem_u32(&bars.v_full[st]), (gp / C::kStages) & 1, ab)) return false;
     tc_fence_after();
-    const uint32_t sV = sbase + C::kOffV + st * C::kTileBytes;
+    const uint64_t vd = smem_desc_sw128(sbase + C::kOffV + st * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t vdesc = smem_desc_sw128(sV + kk * 2048, C::kChunkBytes, 1024);
-      mma_bf16_ts(tmem + C::kColO, tmem + C::kColP + pb * 64 + kk * 8, vdesc, idesc_pv,
+    for (int kk = 0; kk < 8; ++kk)
+      mma_bf16_ts(tmem + C::kColO, tmem + C::kColP + pb * 64 + kk * 8, desc_at(vd, kk * 2048), idesc_pv,
                   (first && kk == 0) ? 0u : 1u);
-    }
     mma_commit(smem_u32(&bars.v_empty[st]));
     mma_commit(smem_u32(&bars.pv_done[pb]));
     return true;
@@ -203,12 +201,12 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
            mbar_wait(smem_u32(&bars.s_empty[sb]), ((gj >> 1) & 1) ^ 1, ab);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
+      const uint64_t kd = smem_desc_sw128(sbase + C::kOffK + st * C::kTileBytes, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-        mma_bf16_ss(tmem + C::kColS + sb * 128, smem_desc_sw128(sQ + koff, 16, 1024),
-                    smem_desc_sw128(sK + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        mma_bf16_ss(tmem + C::kColS + sb * 128, desc_at(qd, koff), desc_at(kd, koff), idesc_qk,
+                    kk > 0 ? 1u : 0u);
       }
       mma_commit(smem_u32(&bars.s_full[sb]));
       mma_commit(smem_u32(&bars.k_empty[st]));

@@ -250,6 +250,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The descriptor of the same operand `byte_off` bytes further on (16-byte
+// aligned offsets; the 14-bit start-address field cannot carry for shared
+// memory addresses below 256 KB).  Building descriptors once per tile and
+// stepping them with one add keeps the issuing thread's instruction count low:
+// it shares its SM sub-partition with softmax warps that keep the issue slots
+// busy.
+__device__ __forceinline__ uint64_t desc_at(uint64_t desc, uint32_t byte_off) {
+  return desc + (byte_off >> 4);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, one elected thread.
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
