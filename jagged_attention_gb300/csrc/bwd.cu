@@ -55,19 +55,21 @@ __global__ void __launch_bounds__(256)
 //   dV   += P^T dO_m                   A = P^T from TMEM
 //   dK   += dS^T Q_m                   A = dS^T, K-major view
 //   dQ_m  = dS K_n                     A = the same dS^T buffer, M-major view
-// dQ_m is drained by WG1 (TMEM -> registers -> fp32 vector reduce-add into
-// dq; in broadcast mode every sequence's tiles add into the same rows: the
-// cross-batch reduction of the GEM page, "GEM's sequences do not fit a fixed
-// grid").  The TMEM slice holding dQ_m is released as soon as it sits in
-// registers, before the global reductions (the pages' early TMEM release).
-// At the end of a tile WG1 writes dV and scale*dK in bf16.
+// dQ_m leaves through the drain group: TMEM -> registers -> swizzled shared
+// staging -> tensor reduce-add into the fp32 dq (in broadcast mode every
+// sequence's tiles add into the same rows: the cross-batch reduction of the
+// GEM page, "GEM's sequences do not fit a fixed grid").  The TMEM slice
+// holding dQ_m is released as soon as it sits in shared memory (the pages'
+// early TMEM release).  At the end of a tile the same group writes dV and
+// scale*dK in bf16.
 //
-//   warps 0-3  WG0: P^T and dS^T (thread = key row)
-//   warps 4-7  WG1: dQ drain (thread = query row), dK / dV epilogue
-//   warp 8     TMA producer: K_n, V_n per tile; Q_m, dO_m double-buffered
-//   warp 9     tcgen05.mma issuer, TMEM owner
-// TMEM: S^T [0,128) (P^T bf16 pairs in its first 64 columns), dP^T [128,256)
-// (dQ_m reuses it), dV [256, 256+D), dK [256+D, 256+2D).
+//   warps 0-7   two softmax groups: P^T and dS^T (thread = key row), query
+//               columns split in halves
+//   warp 8      TMA producer: K_n, V_n per tile; Q_m, dO_m double-buffered
+//   warp 9      tcgen05.mma issuer, TMEM owner
+//   warps 10-13 drain: dQ (thread = query row), dK / dV epilogue
+// TMEM: S^T [0,128) (P^T bf16 pairs in columns [0,32) and [64,96)), dP^T
+// [128,256) (dQ_m reuses it), dV [256, 256+D), dK [256+D, 256+2D).
 // ===========================================================================
 
 template <int D>
