@@ -38,7 +38,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 128 rows x 64 columns (128 bytes) with the 128-byte swizzle the MMA
 // descriptors expect.  Rows past the end read as zeros.  An empty tensor gets
 // a zeroed descriptor that no tile ever uses.
-// box_rows = 32: the unit one warp of the backward stores dK or dV in.
+// box_rows = 32: the unit one warp stores O (forward) or dK / dV (backward) in.
 int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, unsigned box_rows = 128) {
   std::memset(m, 0, sizeof(*m));
   if (rows == 0) return JFA_OK;
@@ -312,9 +312,9 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
     return JFA_ERR_ALIGNMENT;
   if (plan->fwd.P == 0) return JFA_OK;
   const int64_t cols = int64_t(plan->H) * plan->D;
-  CUtensorMap qm, km, vm;
+  CUtensorMap qm, km, vm, om;
   if (make_map(&qm, q, plan->n_q, cols) || make_map(&km, k, plan->n_kv, cols) ||
-      make_map(&vm, v, plan->n_kv, cols))
+      make_map(&vm, v, plan->n_kv, cols) || make_map(&om, out, plan->n_o, cols, 32))
     return JFA_ERR_CUDA;
   jfa::FwdArgs a;
   a.pb = problem_of(plan);
@@ -325,7 +325,7 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
   a.lse = lse;
   a.status = plan->d_status;
   a.packed = plan->packed;
-  cudaError_t e = jfa::launch_fwd(a, qm, km, vm, plan->fwd.P, static_cast<cudaStream_t>(stream));
+  cudaError_t e = jfa::launch_fwd(a, qm, km, vm, om, plan->fwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

@@ -50,7 +50,11 @@ struct FwdCfg {
   // 2 groups x 2 sums x 128 rows)
   static constexpr int kOffXMax = kOffV + kStages * kTileBytes;
   static constexpr int kOffXSum = kOffXMax + 2 * 2 * 128 * 4;
-  static constexpr int kOffBar = kOffXSum + 2 * 2 * 2 * 128 * 4;
+  // O leaves through shared memory at D = 128: per softmax group a
+  // 128-byte-swizzled [128 rows x 64 bf16] box, stored by TMA a warp (32
+  // rows) at a time
+  static constexpr int kOffOStg = kOffXSum + 2 * 2 * 2 * 128 * 4;
+  static constexpr int kOffBar = kOffOStg + (D == 128 ? 2 * 16384 : 0);
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + barriers + alignment slack
   static constexpr uint32_t kColS = 0;               // 2 x 128 fp32 columns
@@ -226,8 +230,8 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
 // softmax / correction / epilogue (warps 0-3, thread = query row = TMEM lane)
 // ---------------------------------------------------------------------------
 template <int D, bool kPack>
-__device__ void fwd_softmax(const FwdArgs& a, uint8_t* smem, uint32_t tmem, FwdBars& bars,
-                            const Abort& ab, int t_begin, int t_end, int grp) {
+__device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t* smem, uint32_t tmem,
+                            FwdBars& bars, const Abort& ab, int t_begin, int t_end, int grp) {
   using C = FwdCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;  // row of the tile, TMEM lane
@@ -364,15 +368,29 @@ __device__ void fwd_softmax(const FwdArgs& a, uint8_t* smem, uint32_t tmem, FwdB
     if (!warp_wait(smem_u32(&bars.pv_done[gl & 1]), (gl >> 1) & 1, ab)) return;
     tc_fence_after();
     const float inv_l = 1.0f / lr_run;
+    // a warp whose 32 rows all belong to the tile stages them for one TMA
+    // store (row-wise scattered 16-byte stores reach a fraction of the memory
+    // system's rate); a warp with rows past the sequence stores its valid rows
+    const bool staged = D == 128 && __all_sync(0xffffffffu, row_ok);
+    const uint32_t stg_warp = smem_u32(smem + C::kOffOStg) + grp * 16384 + (warp & 3) * 4096;
+    if (staged) {
+      if (lane == 0) bulk_wait_read_all();  // this warp's previous O box has been read out
+      __syncwarp();
+    }
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
       uint32_t v[32];
       tmem_ld_x32(tl + C::kColO + o0 + c * 32, v);
-      if (row_ok) {
-        uint32_t w[16];
+      uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
+      for (int e = 0; e < 16; ++e)
+        w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
+      if (staged) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(stg_warp + lane * 128 + (((4 * c + q) ^ (lane & 7)) << 4), w[4 * q], w[4 * q + 1],
+                       w[4 * q + 2], w[4 * q + 3]);
+      } else if (row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(orow_ptr + c * 32);
 #pragma unroll
         for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
@@ -380,6 +398,14 @@ __device__ void fwd_softmax(const FwdArgs& a, uint8_t* smem, uint32_t tmem, FwdB
     }
     tc_fence_before();
     mbar_arrive(smem_u32(&bars.o_empty));
+    if (staged) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(o_map, stg_warp, t.h * D + o0, static_cast<int>(orow - lane));
+        bulk_commit();
+      }
+    }
     if (row_ok && grp == 0) a.lse[int64_t(t.h) * a.pb.n_o + orow] = (m_run + __log2f(l_run)) * kLn2;
     g += t.cost;
     ++tq;
@@ -390,7 +416,8 @@ template <int D, bool kPack>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
-                   const __grid_constant__ CUtensorMap v_map, const FwdArgs a) {
+                   const __grid_constant__ CUtensorMap v_map,
+                   const __grid_constant__ CUtensorMap o_map, const FwdArgs a) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -439,7 +466,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     if (lane == 0) fwd_mma<D>(a, sbase, tmem, bars, ab, t_begin, t_end);
     __syncwarp();
   } else {
-    fwd_softmax<D, kPack>(a, smem, tmem, bars, ab, t_begin, t_end, warp >> 2);
+    fwd_softmax<D, kPack>(a, &o_map, smem, tmem, bars, ab, t_begin, t_end, warp >> 2);
+    if (lane == 0) bulk_wait_all();  // O boxes written before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -451,7 +479,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
 template <int D, bool kPack>
 cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
-                         const CUtensorMap& v, int grid, cudaStream_t stream) {
+                         const CUtensorMap& v, const CUtensorMap& o, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static_assert(sizeof(FwdBars) <= C::kBarBytes, "barrier block");
@@ -462,22 +490,23 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorM
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  jfa_fwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, a);
+  jfa_fwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, o, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
-                       const CUtensorMap& v_map, int grid, cudaStream_t stream) {
+                       const CUtensorMap& v_map, const CUtensorMap& o_map, int grid,
+                       cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   // plans with packed short sequences run an instantiation that handles
   // packed tiles; the others keep the plain code path
   if (a.pb.D == 128)
-    return a.packed ? launch_fwd_d<128, true>(a, q_map, k_map, v_map, grid, stream)
-                    : launch_fwd_d<128, false>(a, q_map, k_map, v_map, grid, stream);
-  return a.packed ? launch_fwd_d<64, true>(a, q_map, k_map, v_map, grid, stream)
-                  : launch_fwd_d<64, false>(a, q_map, k_map, v_map, grid, stream);
+    return a.packed ? launch_fwd_d<128, true>(a, q_map, k_map, v_map, o_map, grid, stream)
+                    : launch_fwd_d<128, false>(a, q_map, k_map, v_map, o_map, grid, stream);
+  return a.packed ? launch_fwd_d<64, true>(a, q_map, k_map, v_map, o_map, grid, stream)
+                  : launch_fwd_d<64, false>(a, q_map, k_map, v_map, o_map, grid, stream);
 }
 
 }  // namespace jfa

@@ -44,9 +44,11 @@ struct BwdArgs {
                            // sequences uncleared: their one tile stores them
 };
 
-// Forward: one persistent launch over the schedule (grid = P CTAs).
+// Forward: one persistent launch over the schedule (grid = P CTAs).  o_map:
+// bf16 O as [rows, H*D] in boxes of 32 rows x 64 columns (128-byte swizzle).
 cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
-                       const CUtensorMap& v_map, int grid, cudaStream_t stream);
+                       const CUtensorMap& v_map, const CUtensorMap& o_map, int grid,
+                       cudaStream_t stream);
 
 // Backward pre-pass: delta[h, i] = sum_d dO[i,h,d] * O[i,h,d].
 cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta, int64_t n_o,
