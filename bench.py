@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from the committed ncu captures (profiles/), keyed by
 # kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 872.5 MB at 256 sequences, x3.730
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2539e9, "src_hash": "1795dfbc2ccb6015"},
-    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 476.5 MB at 256 sequences, x3.730
-    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7772e9, "src_hash": "5f197e1a76c016bc"},
+    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 872.4 MB at 256 sequences, x3.730
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2536e+09, "src_hash": "0b83bca760164ac7"},
+    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 479.1 MB at 256 sequences, x3.730
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7867e+09, "src_hash": "e74ce6eca7b428d5"},
 }
 
 
