@@ -271,7 +271,7 @@ def run_ours(args, rank, world, dist):
     w = workloads.WORKLOADS[args.workload]
     prob = workloads.make_workload(args.workload, seed=args.seed + rank, device=dev,
                                    batch=args.batch)
-    flags = jfa.PLAN_PACK_SHORT if args.pack else 0
+    flags = (jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
     plan = jfa.Plan(prob.kv_offsets, prob.q_offsets, H=prob.H, D=prob.D, Lq=prob.Lq, flags=flags)
     out = torch.empty((prob.n_o_rows, prob.H, prob.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((prob.H, prob.n_o_rows), dtype=torch.float32, device=dev)
@@ -395,7 +395,8 @@ def run_ours(args, rank, world, dist):
                    "sum_kv_tokens": int(prob.kv_offsets[-1]),
                    "l2": f"inputs larger than L2 (K+V {kv_gb:.2f} GB per step), no flush",
                    "parallelism": f"dp{world} (independent batches)",
-                   "plan": "short sequences packed" if args.pack else "plain schedule"},
+                   "plan": ("short sequences packed" if args.pack else "plain schedule")
+                           + (", tiles claimed at run time" if args.dynamic else "")},
         "fwd_tflops": per_kernel["jfa_fwd_kernel"]["tflops"],
         "bwd_tflops": flops(prob, "bwd") / ((k_pre + k_main) / args.steps * 1e-3) / 1e12,
         "pct_bf16_peak": {"fwd": 100 * per_kernel["jfa_fwd_kernel"]["tensor_frac"],
@@ -438,7 +439,8 @@ def run_e2e(args, prob, dev, stream, jfa):
         dv_.copy_(hv, non_blocking=True)
         ddo.copy_(hdo, non_blocking=True)
         plan = jfa.Plan(prob.kv_offsets, prob.q_offsets, H=prob.H, D=prob.D, Lq=prob.Lq,
-                        flags=jfa.PLAN_PACK_SHORT if args.pack else 0, stream=stream)
+                        flags=(jfa.PLAN_PACK_SHORT if args.pack else 0)
+                        | (jfa.PLAN_DYNAMIC if args.dynamic else 0), stream=stream)
         o, l = jfa.fwd(plan, dq_, dk_, dv_, prob.scale, stream=stream)
         g = jfa.bwd(plan, dq_, dk_, dv_, o, ddo, l, prob.scale, stream=stream)
         ho.copy_(o, non_blocking=True)
@@ -470,6 +472,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--dynamic", action="store_true",
+                    help="claim tiles at run time (JFA_PLAN_DYNAMIC) instead of the host deal")
     ap.add_argument("--pack", action="store_true",
                     help="plan with short sequences packed into shared tiles (block-diagonal fast path)")
     ap.add_argument("--batch", type=int, default=None,

@@ -103,6 +103,21 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
  */
 #define JFA_PLAN_PACK_SHORT 1u
 
+/*
+ * JFA_PLAN_DYNAMIC: tiles are claimed at run time instead of dealt on the
+ * host (the pages' dynamic balancing, which "complements" the static order):
+ * each schedule lists every tile once in claim order -- the tiles stably
+ * sorted by their cost field, largest first -- and the plan's P CTAs take
+ * tile blockIdx.x, then the next unclaimed one from a device counter, until
+ * none is left.  jfa_plan_tiles / jfa_build_tiles return that list with
+ * cta_ptr = {0, T, ..., T} (P + 1 entries: one queue shared by the P CTAs
+ * launched).  The
+ * counter lives in the plan and is reset on the stream before each launch,
+ * so a plan's launches must be stream-ordered.  Combines with
+ * JFA_PLAN_PACK_SHORT.
+ */
+#define JFA_PLAN_DYNAMIC 2u
+
 /* jfa_plan_create with flags (0 = the schedule described above). */
 int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                        int Lq, int D, int num_ctas, unsigned flags, void* stream, jfa_plan_t* out);

@@ -29,6 +29,7 @@ STATUS_NAMES = {
 }
 BLOCK_M = BLOCK_N = 128
 PLAN_PACK_SHORT = 1  # JFA_PLAN_PACK_SHORT
+PLAN_DYNAMIC = 2  # JFA_PLAN_DYNAMIC
 
 
 class JfaError(RuntimeError):

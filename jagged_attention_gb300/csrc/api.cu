@@ -144,8 +144,10 @@ int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
   std::vector<int> pack;
   const bool packing = use_packing(flags, kv_offsets_host, q_offsets_host, B);
   if (packing) pack = jfa::short_packs(kvlen);
-  const Schedule s = dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr)
-                              : jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr);
+  const bool dyn = (flags & JFA_PLAN_DYNAMIC) != 0;
+  const Schedule s =
+      dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, dyn)
+               : jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, dyn);
   *T = s.T;
   *P = s.P;
   if (tiles_out) std::memcpy(tiles_out, s.tiles.data(), s.tiles.size() * sizeof(int32_t));
@@ -217,8 +219,9 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
       p->dq_own_rows = true;
     }
   }
-  p->fwd = jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr);
-  p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr);
+  p->dynamic = (flags & JFA_PLAN_DYNAMIC) != 0;
+  p->fwd = jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->dynamic);
+  p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->dynamic);
   for (int b = 0; b < B; ++b) {
     if (qlen[b] == 0 && kvlen[b] > 0) {
       const int64_t s = kv_offsets_host[b], e = kv_offsets_host[b + 1];
@@ -229,7 +232,8 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
     }
   }
 
-  // one device block: offsets, schedules, status word (16-byte aligned pieces)
+  // one device block: offsets, schedules, status word and the two claim
+  // counters of dynamic schedules (16-byte aligned pieces)
   const size_t o_kv = 0;
   const size_t o_q = align_up(o_kv + (B + 1) * 4, 16);
   const size_t o_ft = align_up(o_q + (q_offsets_host ? (B + 1) * 4 : 0), 16);
@@ -265,6 +269,7 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   p->d_bwd_tiles = reinterpret_cast<int32_t*>(base + o_bt);
   p->d_bwd_ptr = reinterpret_cast<int32_t*>(base + o_bp);
   p->d_status = reinterpret_cast<int*>(base + o_st);
+  p->d_counters = reinterpret_cast<int*>(base + o_st + 4);
   *out = p;
   return JFA_OK;
 }
@@ -325,6 +330,12 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
   a.lse = lse;
   a.status = plan->d_status;
   a.packed = plan->packed;
+  a.T = plan->fwd.T;
+  if (plan->dynamic) {
+    a.dyn_counter = plan->d_counters;
+    if (cudaMemsetAsync(a.dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return JFA_ERR_CUDA;
+  }
   cudaError_t e = jfa::launch_fwd(a, qm, km, vm, om, plan->fwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
@@ -404,6 +415,12 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
   a.status = plan->d_status;
   a.packed = plan->packed;
   a.own_rows = plan->dq_own_rows;
+  a.T = plan->bwd.T;
+  if (plan->dynamic) {
+    a.dyn_counter = plan->d_counters + 1;
+    if (cudaMemsetAsync(a.dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return JFA_ERR_CUDA;
+  }
   cudaError_t e =
       jfa::launch_bwd(a, qm, km, vm, dom, dqm, dkm, dvm, plan->bwd.P, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;

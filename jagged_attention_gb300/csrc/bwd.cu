@@ -2,6 +2,7 @@
 #include <algorithm>
 #include "kernels.h"
 #include "sm103_ptx.cuh"
+#include "tiles.cuh"
 
 namespace jfa {
 namespace {
@@ -83,7 +84,8 @@ struct BwdCfg {
   static constexpr int kOffDS = 6 * kTileBytes;       // dS^T [128 keys x 128 queries] bf16
   static constexpr int kOffLse = kOffDS + 32768;      // 128 LSE*log2(e), 128 Delta (fp32)
   static constexpr int kOffBar = kOffLse + 1024;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColDP = 128;
   static constexpr uint32_t kColDV = 256;
@@ -104,6 +106,7 @@ struct BwdBars {
   uint64_t dkv_full, dkv_empty;
   uint64_t lse_ready[2], lse_done[2];  // per softmax group: LSE / Delta staging
   uint64_t drain;
+  TileRing ring;  // dynamic schedules: tile indices from the producer to the other roles
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -127,10 +130,10 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
-template <int D, bool kPack>
+template <int D, bool kPack, class Seq>
 __device__ void bwd_producer(const BwdArgs& a, const CUtensorMap* q_map, const CUtensorMap* k_map,
                              const CUtensorMap* v_map, const CUtensorMap* do_map, uint32_t sbase,
-                             BwdBars& bars, const Abort& ab, int t_begin, int t_end) {
+                             BwdBars& bars, const Abort& ab, Seq& seq) {
   using C = BwdCfg<D>;
   tma_prefetch_desc(q_map);
   tma_prefetch_desc(k_map);
@@ -145,7 +148,8 @@ __device__ void bwd_producer(const BwdArgs& a, const CUtensorMap* q_map, const C
   uint32_t nq = 0, nf[2] = {0, 0};  // Q/dO stage loads, fills per K/V buffer
   bool ok = true;
   uint32_t u = 0;
-  for (int i = t_begin; i < t_end && ok; ++i, ++u) {
+  auto next = [&] { return seq.claim(a.dyn_counter, a.T, bars.ring, ab); };
+  for (int i = next(); i >= 0 && ok; i = next(), ++u) {
     const BTile t = load_btile(a.tiles, i);
     const int x0 = t.h * D;
     const int k_row0 = a.pb.kv_off[t.b] + (kPack ? max(t.n, 0) : t.n) * 128;  // packed tiles: n < 0
@@ -189,9 +193,9 @@ __device__ void bwd_producer(const BwdArgs& a, const CUtensorMap* q_map, const C
 }
 
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, class Seq>
 __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars& bars,
-                        const Abort& ab, int t_begin, int t_end) {
+                        const Abort& ab, Seq& seq) {
   using C = BwdCfg<D>;
   constexpr uint32_t id_sdp = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   constexpr uint32_t id_kmaj = idesc_bf16_f32(128, D, false, true);    // dV (A in TMEM), dK
@@ -200,7 +204,8 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
   const uint64_t dsd_k = smem_desc_sw128(sDS, 16, 1024), dsd_m = smem_desc_sw128(sDS, C::kChunkBytes, 1024);
   uint32_t gm = 0, tt = 0;
   bool ok = true;
-  for (int i = t_begin; i < t_end && ok; ++i) {
+  auto next = [&] { return seq.take(a.dyn_counter, bars.ring, ab); };
+  for (int i = next(); i >= 0 && ok; i = next()) {
     const BTile t = load_btile(a.tiles, i);
     const uint32_t kb = tt & 1, vb = kb ^ 1;  // K and V buffers of this tile
     const uint32_t sK = sbase + C::kOffKV + kb * C::kTileBytes;
@@ -282,9 +287,9 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
 // backward needs no row reduction (LSE and Delta are given), so the halves
 // are independent; splitting them puts two warps on every SM sub-partition,
 // which keeps the exp2 unit and the TMEM traffic busy.
-template <int D, bool kPack>
+template <int D, bool kPack, class Seq>
 __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uint32_t tmem,
-                            BwdBars& bars, const Abort& ab, int t_begin, int t_end, int g) {
+                            BwdBars& bars, const Abort& ab, Seq& seq, int g) {
   using C = BwdCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;  // key row of the tile = TMEM lane
@@ -294,7 +299,8 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
   float* dlt = lse2 + 128;
   const uint32_t lse_ready = smem_u32(&bars.lse_ready[g]), lse_done = smem_u32(&bars.lse_done[g]);
   uint32_t gm = 0;
-  for (int i = t_begin; i < t_end; ++i) {
+  auto next = [&] { return seq.take_warp(a.dyn_counter, bars.ring, ab); };
+  for (int i = next(); i >= 0; i = next()) {
     const BTile t = load_btile(a.tiles, i);
     // packed tile (n = -nseq): key and query rows [off[b], off[b + nseq]) of
     // nseq short sequences; a key row only meets its own sequence's queries
@@ -496,10 +502,10 @@ __device__ __forceinline__ void dq_row_out(float* row, const uint32_t (&v)[32], 
 // returns to the producer when every drain warp's boxes have been read out.
 // A warp whose rows run past the sequence writes its valid rows directly.
 // kSelf: queries have their own offsets, so a tile can own its dQ rows.
-template <int D, bool kPack, bool kSelf>
+template <int D, bool kPack, bool kSelf, class Seq>
 __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUtensorMap* dk_map,
                           const CUtensorMap* dv_map, uint32_t sbase, uint32_t tmem, BwdBars& bars,
-                          const Abort& ab, int t_begin, int t_end) {
+                          const Abort& ab, Seq& seq) {
   using C = BwdCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
@@ -507,7 +513,8 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
   const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
   const int H = a.pb.H;
   uint32_t gm = 0, tt = 0;
-  for (int i = t_begin; i < t_end; ++i) {
+  auto next = [&] { return seq.take_warp(a.dyn_counter, bars.ring, ab); };
+  for (int i = next(); i >= 0; i = next()) {
     const BTile t = load_btile(a.tiles, i);
     // a tile that is the only one touching its dQ rows stores them instead of
     // reduce-adding: a packed tile, or (queries with their own offsets) the one
@@ -577,7 +584,7 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
   }
 }
 
-template <int D, bool kPack, bool kSelf>
+template <int D, bool kPack, bool kSelf, bool kDyn>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     jfa_bwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap do_map,
@@ -590,8 +597,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   BwdBars& bars = *reinterpret_cast<BwdBars*>(smem + C::kOffBar);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t_begin = a.cta_ptr[blockIdx.x], t_end = a.cta_ptr[blockIdx.x + 1];
   if (tid == 0) {
+    tile_ring_init(bars.ring, 1 + 8 + 4);  // consumers: MMA thread, 8 softmax and 4 drain warps
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars.kv_full[b]), 1);
       mbar_init(smem_u32(&bars.kv_empty[b]), 1);
@@ -627,16 +634,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   const Abort ab{&bars.abort_flag, a.status};
+  TileSeq<kDyn> seq(a.cta_ptr, a.dyn_counter);
   if (warp < 8) {
-    bwd_softmax<D, kPack>(a, smem, sbase, tmem, bars, ab, t_begin, t_end, warp >> 2);
+    bwd_softmax<D, kPack>(a, smem, sbase, tmem, bars, ab, seq, warp >> 2);
   } else if (warp >= C::kDrainWarp0) {
-    bwd_drain<D, kPack, kSelf>(a, &dq_map, &dk_map, &dv_map, sbase, tmem, bars, ab, t_begin, t_end);
+    bwd_drain<D, kPack, kSelf>(a, &dq_map, &dk_map, &dv_map, sbase, tmem, bars, ab, seq);
     if (lane == 0) bulk_wait_all();  // dQ, dK, dV boxes written before the CTA exits
   } else if (warp == C::kProducerWarp) {
-    if (lane == 0) bwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, t_begin, t_end);
+    if (lane == 0) bwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, &do_map, sbase, bars, ab, seq);
     __syncwarp();
   } else {
-    if (lane == 0) bwd_mma<D>(a, sbase, tmem, bars, ab, t_begin, t_end);
+    if (lane == 0) bwd_mma<D>(a, sbase, tmem, bars, ab, seq);
     __syncwarp();
   }
   tc_fence_before();
@@ -647,21 +655,34 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool kPack, bool kSelf>
+template <int D, bool kPack, bool kSelf, bool kDyn>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, const CUtensorMap& dO, const CUtensorMap& dq,
                          const CUtensorMap& dk, const CUtensorMap& dv, int grid, cudaStream_t stream) {
   using C = BwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
+  static_assert(sizeof(BwdBars) <= C::kBarBytes, "barrier block");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(jfa_bwd_kernel<D, kPack, kSelf>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(jfa_bwd_kernel<D, kPack, kSelf, kDyn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  jfa_bwd_kernel<D, kPack, kSelf><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, dq, dk, dv, a);
+  jfa_bwd_kernel<D, kPack, kSelf, kDyn><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, dq, dk, dv, a);
   return cudaGetLastError();
+}
+
+// packed plans, owned-dQ plans, reduce-only plans and dynamic schedules run
+// their own instantiations
+template <int D, bool kDyn>
+cudaError_t launch_bwd_m(bool packed, bool self, const BwdArgs& a, const CUtensorMap& q,
+                         const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dO,
+                         const CUtensorMap& dq, const CUtensorMap& dk, const CUtensorMap& dv, int grid,
+                         cudaStream_t stream) {
+  if (packed) return launch_bwd_d<D, true, true, kDyn>(a, q, k, v, dO, dq, dk, dv, grid, stream);
+  if (self) return launch_bwd_d<D, false, true, kDyn>(a, q, k, v, dO, dq, dk, dv, grid, stream);
+  return launch_bwd_d<D, false, false, kDyn>(a, q, k, v, dO, dq, dk, dv, grid, stream);
 }
 
 }  // namespace
@@ -689,12 +710,10 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& q_map, const CUtenso
   // plans where every tile reduce-adds run separate instantiations
   const bool self = a.own_rows;
   if (a.pb.D == 128)
-    return a.packed ? launch_bwd_d<128, true, true>(JFA_BWD_ARGS)
-                    : self ? launch_bwd_d<128, false, true>(JFA_BWD_ARGS)
-                           : launch_bwd_d<128, false, false>(JFA_BWD_ARGS);
-  return a.packed ? launch_bwd_d<64, true, true>(JFA_BWD_ARGS)
-                  : self ? launch_bwd_d<64, false, true>(JFA_BWD_ARGS)
-                         : launch_bwd_d<64, false, false>(JFA_BWD_ARGS);
+    return a.dyn_counter ? launch_bwd_m<128, true>(a.packed, self, JFA_BWD_ARGS)
+                         : launch_bwd_m<128, false>(a.packed, self, JFA_BWD_ARGS);
+  return a.dyn_counter ? launch_bwd_m<64, true>(a.packed, self, JFA_BWD_ARGS)
+                       : launch_bwd_m<64, false>(a.packed, self, JFA_BWD_ARGS);
 #undef JFA_BWD_ARGS
 }
 }  // namespace jfa

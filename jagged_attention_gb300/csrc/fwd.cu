@@ -29,6 +29,7 @@
 // (the pages' "loop peeling": the bulk pass is branch-free).
 #include "kernels.h"
 #include "sm103_ptx.cuh"
+#include "tiles.cuh"
 
 namespace jfa {
 namespace {
@@ -74,6 +75,7 @@ struct FwdBars {
   uint64_t max_ready[2];  // both groups' partial row maxima of a block are in shared memory
   uint64_t sum_ready[2];  // both groups' partial row sums of a tile are in shared memory
   uint64_t drain;
+  TileRing ring;  // dynamic schedules: tile indices from the producer to the other roles
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -103,10 +105,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
-template <int D, bool kPack>
+template <int D, bool kPack, class Seq>
 __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const CUtensorMap* k_map,
                              const CUtensorMap* v_map, uint32_t sbase, FwdBars& bars,
-                             const Abort& ab, int t_begin, int t_end) {
+                             const Abort& ab, Seq& seq) {
   using C = FwdCfg<D>;
   tma_prefetch_desc(q_map);
   tma_prefetch_desc(k_map);
@@ -114,7 +116,8 @@ __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const C
   const uint32_t sQ = sbase + C::kOffQ;
   uint32_t nq = 0, nk = 0, nv = 0;  // loads issued
   bool ok = true;
-  for (int i = t_begin; i < t_end && ok; ++i) {
+  auto next = [&] { return seq.claim(a.dyn_counter, a.T, bars.ring, ab); };
+  for (int i = next(); i >= 0 && ok; i = next()) {
     const Tile t = load_tile(a.tiles, i);
     if (t.cost == 0) continue;
     const int kv0 = a.pb.kv_off[t.b];
@@ -168,9 +171,9 @@ __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const C
 // ---------------------------------------------------------------------------
 // MMA issuer (one thread)
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, class Seq>
 __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars& bars,
-                        const Abort& ab, int t_begin, int t_end) {
+                        const Abort& ab, Seq& seq) {
   using C = FwdCfg<D>;
   constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
@@ -195,7 +198,8 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
   };
 
   bool ok = true;
-  for (int i = t_begin; i < t_end && ok; ++i) {
+  auto next = [&] { return seq.take(a.dyn_counter, bars.ring, ab); };
+  for (int i = next(); i >= 0 && ok; i = next()) {
     const Tile t = load_tile(a.tiles, i);
     if (t.cost == 0) continue;
     ok = mbar_wait(smem_u32(&bars.q_full), tq & 1, ab);
@@ -229,9 +233,9 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
 // ---------------------------------------------------------------------------
 // softmax / correction / epilogue (warps 0-3, thread = query row = TMEM lane)
 // ---------------------------------------------------------------------------
-template <int D, bool kPack>
+template <int D, bool kPack, class Seq>
 __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t* smem, uint32_t tmem,
-                            FwdBars& bars, const Abort& ab, int t_begin, int t_end, int grp) {
+                            FwdBars& bars, const Abort& ab, Seq& seq, int grp) {
   using C = FwdCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;  // row of the tile, TMEM lane
@@ -244,7 +248,8 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
   const int H = a.pb.H;
   uint32_t g = 0, tq = 0;
 
-  for (int i = t_begin; i < t_end; ++i) {
+  auto next = [&] { return seq.take_warp(a.dyn_counter, bars.ring, ab); };
+  for (int i = next(); i >= 0; i = next()) {
     const Tile t = load_tile(a.tiles, i);
     // packed tile (blk = -nseq): rows [off[b], off[b + nseq]) of nseq short
     // sequences, one key block, each row masked to its own sequence's keys
@@ -412,7 +417,7 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
   }
 }
 
-template <int D, bool kPack>
+template <int D, bool kPack, bool kDyn>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
@@ -425,9 +430,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   FwdBars& bars = *reinterpret_cast<FwdBars*>(smem + C::kOffBar);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t_begin = a.cta_ptr[blockIdx.x], t_end = a.cta_ptr[blockIdx.x + 1];
-
   if (tid == 0) {
+    tile_ring_init(bars.ring, 1 + 8);  // consumers: the MMA thread and the 8 softmax warps
     mbar_init(smem_u32(&bars.q_full), 1);
     mbar_init(smem_u32(&bars.q_empty), 1);
     for (int s = 0; s < C::kStages; ++s) {
@@ -458,15 +462,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   const Abort ab{&bars.abort_flag, a.status};
+  TileSeq<kDyn> seq(a.cta_ptr, a.dyn_counter);
 
   if (warp == C::kProducerWarp) {
-    if (lane == 0) fwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, sbase, bars, ab, t_begin, t_end);
+    if (lane == 0) fwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, sbase, bars, ab, seq);
     __syncwarp();
   } else if (warp == C::kMmaWarp) {
-    if (lane == 0) fwd_mma<D>(a, sbase, tmem, bars, ab, t_begin, t_end);
+    if (lane == 0) fwd_mma<D>(a, sbase, tmem, bars, ab, seq);
     __syncwarp();
   } else {
-    fwd_softmax<D, kPack>(a, &o_map, smem, tmem, bars, ab, t_begin, t_end, warp >> 2);
+    fwd_softmax<D, kPack>(a, &o_map, smem, tmem, bars, ab, seq, warp >> 2);
     if (lane == 0) bulk_wait_all();  // O boxes written before the CTA exits
   }
   tc_fence_before();
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool kPack>
+template <int D, bool kPack, bool kDyn>
 cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, const CUtensorMap& o, int grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -485,13 +490,24 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorM
   static_assert(sizeof(FwdBars) <= C::kBarBytes, "barrier block");
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, kPack>,
+    cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, kPack, kDyn>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  jfa_fwd_kernel<D, kPack><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, o, a);
+  jfa_fwd_kernel<D, kPack, kDyn><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, o, a);
   return cudaGetLastError();
+}
+
+// packed plans and dynamic schedules run their own instantiations
+template <int D>
+cudaError_t launch_fwd_m(const FwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
+                         const CUtensorMap& v, const CUtensorMap& o, int grid, cudaStream_t stream) {
+  if (a.dyn_counter)
+    return a.packed ? launch_fwd_d<D, true, true>(a, q, k, v, o, grid, stream)
+                    : launch_fwd_d<D, false, true>(a, q, k, v, o, grid, stream);
+  return a.packed ? launch_fwd_d<D, true, false>(a, q, k, v, o, grid, stream)
+                  : launch_fwd_d<D, false, false>(a, q, k, v, o, grid, stream);
 }
 
 }  // namespace
@@ -503,10 +519,8 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtenso
   // plans with packed short sequences run an instantiation that handles
   // packed tiles; the others keep the plain code path
   if (a.pb.D == 128)
-    return a.packed ? launch_fwd_d<128, true>(a, q_map, k_map, v_map, o_map, grid, stream)
-                    : launch_fwd_d<128, false>(a, q_map, k_map, v_map, o_map, grid, stream);
-  return a.packed ? launch_fwd_d<64, true>(a, q_map, k_map, v_map, o_map, grid, stream)
-                  : launch_fwd_d<64, false>(a, q_map, k_map, v_map, o_map, grid, stream);
+    return launch_fwd_m<128>(a, q_map, k_map, v_map, o_map, grid, stream);
+  return launch_fwd_m<64>(a, q_map, k_map, v_map, o_map, grid, stream);
 }
 
 }  // namespace jfa

@@ -25,6 +25,8 @@ struct FwdArgs {
   float* lse;              // [H, n_o]
   int* status;
   bool packed;             // the schedule may hold packed tiles {b0, h, -nseq, 1}
+  int* dyn_counter = nullptr;  // dynamic schedule: claim counter (zeroed before the launch)
+  int T = 0;                   // tiles in the schedule
 };
 
 struct BwdArgs {
@@ -42,6 +44,8 @@ struct BwdArgs {
   bool packed;             // the schedule may hold packed tiles {b0, h, -nseq, 1}
   bool own_rows = false;   // the pre-pass left the dQ rows of single-key-block
                            // sequences uncleared: their one tile stores them
+  int* dyn_counter = nullptr;  // dynamic schedule: claim counter (zeroed before the launch)
+  int T = 0;                   // tiles in the schedule
 };
 
 // Forward: one persistent launch over the schedule (grid = P CTAs).  o_map:

@@ -55,8 +55,25 @@ std::vector<int> short_packs(const std::vector<int64_t>& len) {
   return pack;
 }
 
+// Dynamic schedules: the tiles in claim order, one queue for every CTA.
+static Schedule claim_order(const std::vector<int32_t>& flat, int num_ctas) {
+  Schedule s;
+  s.T = static_cast<int>(flat.size() / 4);
+  s.P = std::min(num_ctas, s.T);
+  s.cta_ptr.assign(s.P + 1, s.T);  // one queue: [0, T), the same for every CTA
+  s.cta_ptr[0] = 0;
+  std::vector<int> order(s.T);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return flat[4 * a + 3] > flat[4 * b + 3]; });
+  s.tiles.resize(4 * static_cast<size_t>(s.T));
+  for (int i = 0; i < s.T; ++i)
+    std::copy_n(&flat[4 * static_cast<size_t>(order[i])], 4, &s.tiles[4 * static_cast<size_t>(i)]);
+  return s;
+}
+
 Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
-                            int H, int num_ctas, const std::vector<int>* pack) {
+                            int H, int num_ctas, const std::vector<int>* pack, bool dynamic) {
   const int B = static_cast<int>(q_len.size());
   std::vector<int32_t> flat;  // enumeration order
   for (int b = 0; b < B; ++b) {
@@ -80,6 +97,7 @@ Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector
         flat.push_back(cost);
       }
   }
+  if (dynamic) return claim_order(flat, num_ctas);
   Schedule s;
   s.T = static_cast<int>(flat.size() / 4);
   s.P = std::min(num_ctas, s.T);
@@ -107,7 +125,7 @@ Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector
 }
 
 Schedule build_bwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
-                            int H, int num_ctas, const std::vector<int>* pack) {
+                            int H, int num_ctas, const std::vector<int>* pack, bool dynamic) {
   const int B = static_cast<int>(q_len.size());
   std::vector<int32_t> flat;
   for (int b = 0; b < B; ++b) {
@@ -132,6 +150,7 @@ Schedule build_bwd_schedule(const std::vector<int64_t>& q_len, const std::vector
         flat.push_back(qblocks);
       }
   }
+  if (dynamic) return claim_order(flat, num_ctas);
   Schedule s;
   s.T = static_cast<int>(flat.size() / 4);
   s.P = std::min(num_ctas, s.T);

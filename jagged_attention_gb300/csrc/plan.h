@@ -32,13 +32,17 @@ std::vector<int> short_packs(const std::vector<int64_t>& len);
 // Forward schedule: tiles (b, h, m) for m < ceil(Lq_b / BM) with cost
 // ceil(Lk_b / BN), stable-sorted by cost descending, dealt zigzag to
 // P = min(num_ctas, T) CTAs.
-// `pack` (optional) replaces packed runs by one tile each.
+// `pack` (optional) replaces packed runs by one tile each.  dynamic: instead
+// of the deal, every tile once in claim order (stable sort by the last field,
+// descending) with cta_ptr = {0, T, ..., T}; the CTAs claim tiles at run time.
 Schedule build_fwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
-                            int H, int num_ctas, const std::vector<int>* pack = nullptr);
+                            int H, int num_ctas, const std::vector<int>* pack = nullptr,
+                            bool dynamic = false);
 // Backward schedule: tiles (b, h, n) for n < ceil(Lk_b / BN) where Lq_b > 0,
-// cost ceil(Lq_b / BM), dealt round-robin.
+// cost ceil(Lq_b / BM), dealt round-robin (or in claim order, as above).
 Schedule build_bwd_schedule(const std::vector<int64_t>& q_len, const std::vector<int64_t>& kv_len,
-                            int H, int num_ctas, const std::vector<int>* pack = nullptr);
+                            int H, int num_ctas, const std::vector<int>* pack = nullptr,
+                            bool dynamic = false);
 
 }  // namespace jfa
 
@@ -53,6 +57,8 @@ struct jfa_plan {
   // stores its rows)
   std::vector<std::pair<int64_t, int64_t>> dq_rows_to_clear;
   bool dq_own_rows = false;  // some rows are left to the tiles that own them
+  bool dynamic = false;      // tiles claimed at run time (JFA_PLAN_DYNAMIC)
+  int* d_counters = nullptr; // dynamic: claim counters [fwd, bwd]
   int device = 0;
   int num_ctas = 0;
   int64_t n_q = 0;   // rows of Q

@@ -70,7 +70,7 @@ def short_packs(lengths, limit: int = 128):
     return pack
 
 
-def fwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pack=None):
+def fwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pack=None, dynamic=False):
     tiles = []
     for b in range(len(q_lengths)):
         if pack is not None and pack[b] != 1:
@@ -81,6 +81,8 @@ def fwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pa
         for h in range(H):
             for m in range(_ceil_div(int(q_lengths[b]), BM)):
                 tiles.append((b, h, m, cost))
+    if dynamic:
+        return claim_order(tiles, num_ctas)
     order = sorted(range(len(tiles)), key=lambda i: -tiles[i][3])  # sorted() is stable
     T = len(tiles)
     P = min(num_ctas, T)
@@ -92,7 +94,20 @@ def fwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pa
     return _csr(per_cta, P)
 
 
-def bwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pack=None):
+def claim_order(tiles, num_ctas: int):
+    """Dynamic schedules: every tile once, stably sorted by its last field
+    (cost) descending, one queue for all P = min(num_ctas, T) CTAs:
+    cta_ptr = [0, T, ..., T]."""
+    order = sorted(range(len(tiles)), key=lambda i: -tiles[i][3])  # sorted() is stable
+    T = len(tiles)
+    P = min(num_ctas, T)
+    flat = np.asarray([tiles[i] for i in order], dtype=np.int32).reshape(-1, 4)
+    ptr = np.full(P + 1, T, dtype=np.int32)
+    ptr[0] = 0
+    return flat, ptr
+
+
+def bwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pack=None, dynamic=False):
     tiles = []
     for b in range(len(q_lengths)):
         if pack is not None and pack[b] != 1:
@@ -105,6 +120,8 @@ def bwd_tiles(q_lengths, kv_lengths, H: int, BM: int, BN: int, num_ctas: int, pa
         for h in range(H):
             for n in range(_ceil_div(int(kv_lengths[b]), BN)):
                 tiles.append((b, h, n, qblocks))
+    if dynamic:
+        return claim_order(tiles, num_ctas)
     T = len(tiles)
     P = min(num_ctas, T)
     per_cta = [[] for _ in range(P)]

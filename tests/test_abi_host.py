@@ -25,9 +25,9 @@ def test_exports_every_declared_function():
         assert hasattr(L, n), n
 
 
-def _ref(qlen, klen, H, P, direction, pack=None):
+def _ref(qlen, klen, H, P, direction, pack=None, dynamic=False):
     fn = ref_tiles.fwd_tiles if direction == 0 else ref_tiles.bwd_tiles
-    return fn(qlen, klen, H, 128, 128, P, pack)
+    return fn(qlen, klen, H, 128, 128, P, pack, dynamic)
 
 
 @pytest.mark.parametrize("case", load_cases(), ids=lambda c: c["name"])
@@ -62,6 +62,21 @@ def test_native_builder_matches_reference_random(seed):
         t, p = jfa.build_tiles(kv, qo, H=H, Lq=Lq, num_ctas=P, direction=d)
         rt, rp = _ref(qlen, klen, H, P, d)
         assert np.array_equal(t, rt) and np.array_equal(p, rp)
+        t, p = jfa.build_tiles(kv, qo, H=H, Lq=Lq, num_ctas=P, direction=d, flags=jfa.PLAN_DYNAMIC)
+        rt, rp = _ref(qlen, klen, H, P, d, dynamic=True)
+        assert np.array_equal(t, rt) and np.array_equal(p, rp)
+
+
+def test_dynamic_schedule_lists_every_tile_once_in_cost_order():
+    lens = np.array([60, 40, 30, 200, 64, 64, 1000, 0, 129])
+    kv = workloads.offsets_from_lengths(lens)
+    for flags in (jfa.PLAN_DYNAMIC, jfa.PLAN_DYNAMIC | jfa.PLAN_PACK_SHORT):
+        for d in (0, 1):
+            t, p = jfa.build_tiles(kv, kv, H=3, num_ctas=5, direction=d, flags=flags)
+            static, _ = jfa.build_tiles(kv, kv, H=3, num_ctas=5, direction=d, flags=flags & jfa.PLAN_PACK_SHORT)
+            assert p[0] == 0 and (p[1:] == len(t)).all() and len(p) == min(5, len(t)) + 1
+            assert (np.diff(t[:, 3]) <= 0).all()
+            assert sorted(map(tuple, t)) == sorted(map(tuple, static))
 
 
 @pytest.mark.parametrize("name", sorted(workloads.WORKLOADS))

@@ -37,7 +37,8 @@ def _sampled_sequences(p, rng, n_random=3):
 
 
 @pytest.mark.parametrize("name,flags", [("gem_broadcast", 0), ("skewed_broadcast", 0),
-                                        ("block_diag", 0), ("block_diag", 1)])
+                                        ("block_diag", 0), ("block_diag", 1),
+                                        ("gem_broadcast", 2), ("block_diag", 3)])
 def test_full_size_sampled_parity(name, flags):
     torch.cuda.empty_cache()
     orc = oracle.default()

@@ -11,9 +11,11 @@ BM = BN = 128
 
 @pytest.mark.parametrize("case", load_cases(), ids=lambda c: c["name"])
 def test_reference_builder_matches_hand_worked(case):
-    pack = tiles.short_packs(case["kv_lengths"]) if case.get("flags", 0) else None
-    ft, fp = tiles.fwd_tiles(case["q_lengths"], case["kv_lengths"], case["H"], BM, BN, case["num_ctas"], pack)
-    bt, bp = tiles.bwd_tiles(case["q_lengths"], case["kv_lengths"], case["H"], BM, BN, case["num_ctas"], pack)
+    flags = case.get("flags", 0)
+    pack = tiles.short_packs(case["kv_lengths"]) if flags & 1 else None
+    dyn = bool(flags & 2)
+    ft, fp = tiles.fwd_tiles(case["q_lengths"], case["kv_lengths"], case["H"], BM, BN, case["num_ctas"], pack, dyn)
+    bt, bp = tiles.bwd_tiles(case["q_lengths"], case["kv_lengths"], case["H"], BM, BN, case["num_ctas"], pack, dyn)
     assert np.array_equal(fp, case["fwd_cta_ptr"]) and np.array_equal(ft, case["fwd"])
     assert np.array_equal(bp, case["bwd_cta_ptr"]) and np.array_equal(bt, case["bwd"])
 
