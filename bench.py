@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from the committed ncu captures (profiles/), keyed by
 # kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 872.4 MB at 256 sequences, x3.730
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2536e+09, "src_hash": "0b83bca760164ac7"},
-    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 479.1 MB at 256 sequences, x3.730
-    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7867e+09, "src_hash": "e74ce6eca7b428d5"},
+    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 872.3 MB at 256 sequences, x3.730
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2533e+09, "src_hash": "5bdbfbce5019494f"},
+    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 479.4 MB at 256 sequences, x3.730
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7881e+09, "src_hash": "e0dc6ab0b9bfb27d"},
 }
 
 
@@ -123,7 +123,13 @@ def alg_bytes(prob, which: str, pack: bool = False) -> float:
 
 
 def src_hash(name: str) -> str:
-    return hashlib.sha256((ROOT / "jagged_attention_gb300" / "csrc" / name).read_bytes()).hexdigest()[:16]
+    """Hash of a kernel's source file and the local headers it includes, so that
+    stored ncu traffic goes stale whenever any code the kernel compiles from changes."""
+    csrc = ROOT / "jagged_attention_gb300" / "csrc"
+    h = hashlib.sha256()
+    for f in (name, "kernels.h", "sm103_ptx.cuh", "tiles.cuh"):
+        h.update((csrc / f).read_bytes())
+    return h.hexdigest()[:16]
 
 
 class ClockSampler:
