@@ -415,9 +415,10 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
 // rows all belong to the tile writes them into shared memory in the
 // 128-byte-swizzled box layout (dV in the Q stage, dK in the dO stage of the
 // step just finished, 64-column chunks 16 KB apart) and stores them as D/64
-// boxes of 32 x 64 each; a warp with rows past the sequence stores its valid
-// rows directly.  Returns whether this warp staged (its lane 0 then owns an
-// open bulk group reading the stage).
+// boxes of 32 x 64 each, dV's boxes leaving while dK is staged; a warp with
+// rows past the sequence stores its valid rows directly.  TMEM is read two
+// 32-column loads per wait.  Returns whether this warp staged (its lane 0
+// then owns open bulk groups reading the stage).
 template <int D, bool kPack>
 __device__ __forceinline__ bool dkv_epilogue(const BwdArgs& a, const CUtensorMap* dk_map,
                                              const CUtensorMap* dv_map, uint32_t sbase, uint32_t qs,
@@ -432,49 +433,53 @@ __device__ __forceinline__ bool dkv_epilogue(const BwdArgs& a, const CUtensorMap
   const bool kv_ok = int64_t(nb) * 128 + r < klen;
   const bool whole = __all_sync(0xffffffffu, kv_ok);
   const int64_t krow = int64_t(a.pb.kv_off[t.b]) + nb * 128 + r;
+  const int y = static_cast<int>(int64_t(a.pb.kv_off[t.b]) + nb * 128 + wq * 32);  // first row of the boxes
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
     const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
     const float mul = which == 0 ? 1.0f : a.scale;
     uint16_t* dst_row = (which == 0 ? a.dv : a.dk) + (krow * H + t.h) * D;
-    const uint32_t stage = sbase + (which == 0 ? C::kOffQ : C::kOffDO) + qs * C::kTileBytes + wq * 4096 +
-                           lane * 128;
+    const uint32_t region = sbase + (which == 0 ? C::kOffQ : C::kOffDO) + qs * C::kTileBytes + wq * 4096;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t w[32];
-      tmem_ld_x32(tl + col + c * 32, w);
-      uint32_t pk[16];
+    for (int c2 = 0; c2 < D / 32; c2 += 2) {
+      uint32_t ww[2][32];
+      tmem_ld_x32_nw(tl + col + c2 * 32, ww[0]);
+      tmem_ld_x32_nw(tl + col + (c2 + 1) * 32, ww[1]);
+      tmem_ld_wait2(ww[0], ww[1]);
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pk[e] = pack_bf16x2(__uint_as_float(w[2 * e]) * mul, __uint_as_float(w[2 * e + 1]) * mul);
-      if (whole) {
-        // 32 columns = units 4(c&1) .. 4(c&1)+3 of the row in chunk c/2
-        const uint32_t dst = stage + (c >> 1) * 16384;
+      for (int h = 0; h < 2; ++h) {
+        const int c = c2 + h;
+        uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_shared_v4(dst + (((4 * (c & 1) + q) ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
-                       pk[4 * q + 2], pk[4 * q + 3]);
-      } else if (kv_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(ww[h][2 * e]) * mul, __uint_as_float(ww[h][2 * e + 1]) * mul);
+        if (whole) {
+          // 32 columns = units 4(c&1) .. 4(c&1)+3 of the row in chunk c/2
+          const uint32_t dst = region + lane * 128 + (c >> 1) * 16384;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            st_shared_v4(dst + (((4 * (c & 1) + q) ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                         pk[4 * q + 2], pk[4 * q + 3]);
+        } else if (kv_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
       }
     }
-  }
-  tc_fence_before();
-  mbar_arrive(dkv_empty);  // dK / dV TMEM columns free for the next tile
-  if (whole) {
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      const int y = static_cast<int>(int64_t(a.pb.kv_off[t.b]) + nb * 128 + wq * 32);
+    if (which == 1) {
+      tc_fence_before();
+      mbar_arrive(dkv_empty);  // dK / dV TMEM columns free for the next tile
+    }
+    if (whole) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const uint32_t off = qs * C::kTileBytes + wq * 4096 + c * 16384;
-        tma_store_2d(dv_map, sbase + C::kOffQ + off, t.h * D + c * 64, y);
-        tma_store_2d(dk_map, sbase + C::kOffDO + off, t.h * D + c * 64, y);
+        for (int c = 0; c < D / 64; ++c)
+          tma_store_2d(which == 0 ? dv_map : dk_map, region + c * 16384, t.h * D + c * 64, y);
+        bulk_commit();
       }
-      bulk_commit();
     }
   }
   return whole;
@@ -496,7 +501,8 @@ __device__ __forceinline__ void dq_row_out(float* row, const uint32_t (&v)[32], 
 // scattered 16-byte pieces at a fraction of the rate of whole rows.  So each
 // drain warp writes its 32 rows into shared memory in the 128-byte-swizzled
 // box layout and hands them to the tensor-memory-access unit as D/32 boxes of
-// 32 x 32 fp32 (reduce-add, or store when the tile owns the rows).  The staging space is
+// 32 x 32 fp32 (reduce-add, or store when the tile owns the rows), reading
+// TMEM two 32-column loads per wait.  The staging space is
 // the Q/dO stage of the step just finished, free once dq_full has fired: its
 // D/32 boxes of 16 KB fill the Q stage first, then the dO stage.  The stage
 // returns to the producer when every drain warp's boxes have been read out.
@@ -546,20 +552,27 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
                wq * 4096;
       };
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
-        uint32_t v[32];
-        tmem_ld_x32(tl + C::kColDP + k * 32, v);
-        if (whole) {
-          const uint32_t dst = box_addr(k) + lane * 128;
+      for (int k2 = 0; k2 < D / 32; k2 += 2) {
+        uint32_t vv[2][32];
+        tmem_ld_x32_nw(tl + C::kColDP + k2 * 32, vv[0]);
+        tmem_ld_x32_nw(tl + C::kColDP + (k2 + 1) * 32, vv[1]);
+        tmem_ld_wait2(vv[0], vv[1]);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            st_shared_v4(dst + ((u ^ (lane & 7)) << 4),
-                         __float_as_uint(__uint_as_float(v[4 * u]) * a.scale),
-                         __float_as_uint(__uint_as_float(v[4 * u + 1]) * a.scale),
-                         __float_as_uint(__uint_as_float(v[4 * u + 2]) * a.scale),
-                         __float_as_uint(__uint_as_float(v[4 * u + 3]) * a.scale));
-        } else if (q_ok) {
-          dq_row_out(row + k * 32, v, a.scale, store);
+        for (int h = 0; h < 2; ++h) {
+          const int k = k2 + h;
+          const uint32_t (&v)[32] = vv[h];
+          if (whole) {
+            const uint32_t dst = box_addr(k) + lane * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              st_shared_v4(dst + ((u ^ (lane & 7)) << 4),
+                           __float_as_uint(__uint_as_float(v[4 * u]) * a.scale),
+                           __float_as_uint(__uint_as_float(v[4 * u + 1]) * a.scale),
+                           __float_as_uint(__uint_as_float(v[4 * u + 2]) * a.scale),
+                           __float_as_uint(__uint_as_float(v[4 * u + 3]) * a.scale));
+          } else if (q_ok) {
+            dq_row_out(row + k * 32, v, a.scale, store);
+          }
         }
       }
       tc_fence_before();
