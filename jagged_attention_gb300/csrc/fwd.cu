@@ -290,12 +290,15 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
       if (!warp_wait(smem_u32(&bars.s_full[sb]), (gj >> 1) & 1, ab)) return;
       tc_fence_after();
       float s[64];
+      {  // both halves of this group's columns, one wait
+        uint32_t vv[2][32];
+        tmem_ld_x32_nw(tl + C::kColS + sb * 128 + c0, vv[0]);
+        tmem_ld_x32_nw(tl + C::kColS + sb * 128 + c0 + 32, vv[1]);
+        tmem_ld_wait2(vv[0], vv[1]);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld_x32(tl + C::kColS + sb * 128 + c0 + c * 32, v);
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
+          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(vv[c][e]);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.s_empty[sb]));
