@@ -327,17 +327,28 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
       const float m_new = resc ? m_cand : m_run;
       const float alpha = resc ? fast_exp2(m_run - m_new) : 1.0f;
       uint32_t p[32];
-      float rowsum = 0.0f, rowsum_r = 0.0f;
+      uint64_t acc = f2_pack(0.0f, 0.0f), acc_r = f2_pack(0.0f, 0.0f);
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm = f2_pack(-m_new, -m_new);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float p0 = fast_exp2(fmaf(s[2 * e], sl2, -m_new));
-        const float p1 = fast_exp2(fmaf(s[2 * e + 1], sl2, -m_new));
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), sl2x2, negm), x0, x1);
+        const float p0 = fast_exp2(x0);
+        const float p1 = fast_exp2(x1);
         p[e] = pack_bf16x2(p0, p1);
-        rowsum += p0 + p1;
+        acc = f2_add(acc, f2_pack(p0, p1));
         // O is normalised by the sum of the rounded weights the PV product
         // uses (an exact convex combination of V rows under those weights);
         // LSE keeps the sum of the unrounded ones
-        rowsum_r += __uint_as_float(p[e] << 16) + __uint_as_float(p[e] & 0xffff0000u);
+        acc_r = f2_add(acc_r, f2_pack(__uint_as_float(p[e] << 16), __uint_as_float(p[e] & 0xffff0000u)));
+      }
+      float rowsum, rowsum_r;
+      {
+        float a0, a1;
+        f2_unpack(acc, a0, a1);
+        rowsum = a0 + a1;
+        f2_unpack(acc_r, a0, a1);
+        rowsum_r = a0 + a1;
       }
       l_run = l_run * alpha + rowsum;
       lr_run = lr_run * alpha + rowsum_r;
