@@ -387,8 +387,11 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
         for (int e = 0; e < 16; ++e) {
           const int j = c0 + c * 32 + 2 * e;
           const uint32_t pp = p[c * 16 + e];
-          const float d0 = __uint_as_float(pp << 16) * (__uint_as_float(v[2 * e]) - dlt[j]);
-          const float d1 = __uint_as_float(pp & 0xffff0000u) * (__uint_as_float(v[2 * e + 1]) - dlt[j + 1]);
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u)),
+                           f2_sub(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                  *reinterpret_cast<const uint64_t*>(dlt + j))),
+                    d0, d1);
           w[e] = pack_bf16x2(d0, d1);
         }
 #pragma unroll
