@@ -327,7 +327,8 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
       const float m_new = resc ? m_cand : m_run;
       const float alpha = resc ? fast_exp2(m_run - m_new) : 1.0f;
       uint32_t p[32];
-      uint64_t acc = f2_pack(0.0f, 0.0f), acc_r = f2_pack(0.0f, 0.0f);
+      uint64_t acc = f2_pack(0.0f, 0.0f);
+      float r_lo = 0.0f, r_hi = 0.0f;
       const uint64_t sl2x2 = f2_pack(sl2, sl2), negm = f2_pack(-m_new, -m_new);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
@@ -340,15 +341,14 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
         // O is normalised by the sum of the rounded weights the PV product
         // uses (an exact convex combination of V rows under those weights);
         // LSE keeps the sum of the unrounded ones
-        acc_r = f2_add(acc_r, f2_pack(__uint_as_float(p[e] << 16), __uint_as_float(p[e] & 0xffff0000u)));
+        acc_bf16x2(p[e], r_lo, r_hi);
       }
       float rowsum, rowsum_r;
       {
         float a0, a1;
         f2_unpack(acc, a0, a1);
         rowsum = a0 + a1;
-        f2_unpack(acc_r, a0, a1);
-        rowsum_r = a0 + a1;
+        rowsum_r = r_lo + r_hi;
       }
       l_run = l_run * alpha + rowsum;
       lr_run = lr_run * alpha + rowsum_r;

@@ -342,6 +342,13 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+// lo_acc += low bf16 of w, hi_acc += high bf16 of w (fp32 sums of bf16
+// values; the conversion is exact, so this equals shifting each half into a
+// float first).
+__device__ __forceinline__ void acc_bf16x2(uint32_t w, float& lo_acc, float& hi_acc) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(lo_acc), "+f"(hi_acc) : "r"(w));
+}
 __device__ __forceinline__ float fast_exp2(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
