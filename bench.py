@@ -230,6 +230,35 @@ class OracleSample:
 
 
 # ---------------------------------------------------------------------------
+# Multi-rank host logic (weak scaling: every rank runs an independent batch of
+# the same shape; nothing is exchanged on the data path).
+def rank_seed(seed: int, rank: int) -> int:
+    """The seed of rank `rank`'s batch: same workload shape, its own data."""
+    return seed + rank
+
+
+def combine_over_ranks(dist, times, device="cpu"):
+    """Max over ranks of each timing: the slowest rank sets the job's time."""
+    t = torch.tensor(list(times), dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def sum_over_ranks(dist, x: float, device="cpu") -> float:
+    """Sum over ranks (each rank's batch has its own lengths, so its own flops)."""
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return t.item()
+
+
+def aggregate_tflops(job_flops_per_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's work per step over the (max) step time."""
+    return job_flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
 def run_reference(args, rank, world):
     """The oracle, as it stands, on the host cores (rank 0 only)."""
     if rank != 0:
@@ -275,7 +304,7 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     jfa.lib()
     w = workloads.WORKLOADS[args.workload]
-    prob = workloads.make_workload(args.workload, seed=args.seed + rank, device=dev,
+    prob = workloads.make_workload(args.workload, seed=rank_seed(args.seed, rank), device=dev,
                                    batch=args.batch)
     flags = (jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
     plan = jfa.Plan(prob.kv_offsets, prob.q_offsets, H=prob.H, D=prob.D, Lq=prob.Lq, flags=flags)
@@ -324,24 +353,19 @@ def run_ours(args, rank, world, dist):
     k_fwd = sum(e[0].elapsed_time(e[1]) for e in evs)
     k_pre = sum(e[1].elapsed_time(e[2]) for e in evs)
     k_main = sum(e[2].elapsed_time(e[3]) for e in evs)
-    t = torch.tensor([total_ms, k_fwd, k_pre, k_main], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, k_fwd, k_pre, k_main = t.tolist()
+    total_ms, k_fwd, k_pre, k_main = combine_over_ranks(dist, [total_ms, k_fwd, k_pre, k_main], dev)
     ms_step = total_ms / args.steps
 
     fl_step = flops(prob, "fwd") + flops(prob, "bwd")
-    value = world * fl_step / (ms_step * 1e-3) / 1e12
+    fl_job = sum_over_ranks(dist, fl_step, dev)
+    value = aggregate_tflops(fl_job, ms_step)
 
     # ---- end to end through the public API with host buffers ------------------
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, prob, dev, stream, jfa)
-        if dist is not None:
-            tt = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e["ms_per_step"] = tt.item()
-        e2e["value"] = world * fl_step / (e2e["ms_per_step"] * 1e-3) / 1e12
+        e2e["ms_per_step"] = combine_over_ranks(dist, [e2e["ms_per_step"]], dev)[0]
+        e2e["value"] = aggregate_tflops(fl_job, e2e["ms_per_step"])
 
     if rank != 0:
         return
