@@ -82,7 +82,7 @@ struct BwdCfg {
   static constexpr int kOffQ = 2 * kTileBytes;        // 2 stages
   static constexpr int kOffDO = 4 * kTileBytes;       // 2 stages
   static constexpr int kOffDS = 6 * kTileBytes;       // dS^T [128 keys x 128 queries] bf16
-  static constexpr int kOffLse = kOffDS + 32768;      // 128 LSE*log2(e), 128 Delta (fp32)
+  static constexpr int kOffLse = kOffDS + 32768;      // 128 -LSE*log2(e), 128 Delta (fp32)
   static constexpr int kOffBar = kOffLse + 1024;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;
@@ -295,7 +295,7 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
   const int r = (warp & 3) * 32 + lane;  // key row of the tile = TMEM lane
   const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int c0 = 64 * g;                 // first query column of this group
-  float* lse2 = reinterpret_cast<float*>(smem + C::kOffLse);  // 128 LSE*log2(e), then 128 Delta
+  float* lse2 = reinterpret_cast<float*>(smem + C::kOffLse);  // 128 -LSE*log2(e), then 128 Delta
   float* dlt = lse2 + 128;
   const uint32_t lse_ready = smem_u32(&bars.lse_ready[g]), lse_done = smem_u32(&bars.lse_done[g]);
   uint32_t gm = 0;
@@ -328,7 +328,7 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
         const int64_t q = int64_t(m) * 128 + c0 + r;
         const bool q_ok = q < qlen;
         const int64_t idx = int64_t(t.h) * a.pb.n_o + o_base + q;
-        lse2[c0 + r] = q_ok ? a.lse[idx] * 1.4426950408889634f : INFINITY;
+        lse2[c0 + r] = q_ok ? -(a.lse[idx] * 1.4426950408889634f) : -INFINITY;  // -LSE, log2 units
         dlt[c0 + r] = q_ok ? a.delta[idx] : 0.0f;
       }
       mbar_arrive(lse_ready);
@@ -336,39 +336,39 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
 
       if (!warp_wait_b(smem_u32(&bars.s_full), gm & 1, ab)) return;
       tc_fence_after();
-      uint32_t p[32];  // this row's 64 P^T values, bf16 pairs
-      if (!packed) {
+      // P^T goes back into TMEM a 32-column half at a time, over this group's
+      // own S columns read in the first half
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld_x32(tl + C::kColS + c0 + c * 32, v);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld_x32(tl + C::kColS + c0 + c * 32, v);
+        uint32_t ph[16];
+        if (!packed) {
+          const uint64_t sl2x2 = f2_pack(a.scale_log2, a.scale_log2);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = c0 + c * 32 + 2 * e;
-            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, -lse2[j]));
-            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, -lse2[j + 1]));
+            float p0, p1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2x2,
+                             *reinterpret_cast<const uint64_t*>(lse2 + j)), p0, p1);
+            p0 = fast_exp2(p0);
+            p1 = fast_exp2(p1);
             if (!kv_ok) p0 = p1 = 0.0f;
-            p[c * 16 + e] = pack_bf16x2(p0, p1);
+            ph[e] = pack_bf16x2(p0, p1);
           }
-        }
-      } else {  // packed tile: only this key row's own sequence
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld_x32(tl + C::kColS + c0 + c * 32, v);
+        } else {  // packed tile: only this key row's own sequence
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = c0 + c * 32 + 2 * e;
-            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, -lse2[j]));
-            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, -lse2[j + 1]));
+            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, lse2[j]));
+            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, lse2[j + 1]));
             if (!kv_ok || j < q_lo || j >= q_hi) p0 = 0.0f;
             if (!kv_ok || j + 1 < q_lo || j + 1 >= q_hi) p1 = 0.0f;
-            p[c * 16 + e] = pack_bf16x2(p0, p1);
+            ph[e] = pack_bf16x2(p0, p1);
           }
         }
+        tmem_st_x16(tl + C::kColS + c0 + c * 16, ph);
       }
-      // P^T back into TMEM over this group's own (already read) S columns
-      tmem_st_x32(tl + C::kColS + c0, p);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full));
@@ -378,10 +378,17 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
       if (!warp_wait_b(smem_u32(&bars.ds_empty), (gm & 1) ^ 1, ab)) return;
       tc_fence_after();
       const uint32_t sDS = sbase + C::kOffDS + g * C::kChunkBytes;  // 128-byte chunk g of each row
+      uint32_t p[32];  // P^T of this row, back from TMEM
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld_x32(tl + C::kColDP + c0 + c * 32, v);
+        if (c == 0) {
+          tmem_ld_x32_nw(tl + C::kColS + c0, p);
+          tmem_ld_x32_nw(tl + C::kColDP + c0, v);
+          tmem_ld_wait2(p, v);
+        } else {
+          tmem_ld_x32(tl + C::kColDP + c0 + 32, v);
+        }
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
