@@ -45,9 +45,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
     # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 872.2 MB at 256 sequences, x3.730
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2531e+09, "src_hash": "acdf9050f7fa2d93"},
-    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 478.8 MB at 256 sequences, x3.730
-    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7856e+09, "src_hash": "ca5eed8b3c7fe6fd"},
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2531e+09, "src_hash": "ffe128e04d76b9b2"},
+    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 479.0 MB at 256 sequences, x3.730
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7865e+09, "src_hash": "ca5eed8b3c7fe6fd"},
 }
 
 
