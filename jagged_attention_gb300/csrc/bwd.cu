@@ -358,10 +358,14 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
           }
         } else {  // packed tile: only this key row's own sequence
 #pragma unroll
+          const uint64_t sl2x2 = f2_pack(a.scale_log2, a.scale_log2);
           for (int e = 0; e < 16; ++e) {
             const int j = c0 + c * 32 + 2 * e;
-            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), a.scale_log2, lse2[j]));
-            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), a.scale_log2, lse2[j + 1]));
+            float p0, p1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2x2,
+                             *reinterpret_cast<const uint64_t*>(lse2 + j)), p0, p1);
+            p0 = fast_exp2(p0);
+            p1 = fast_exp2(p1);
             if (!kv_ok || j < q_lo || j >= q_hi) p0 = 0.0f;
             if (!kv_ok || j + 1 < q_lo || j + 1 >= q_hi) p1 = 0.0f;
             ph[e] = pack_bf16x2(p0, p1);

@@ -396,10 +396,19 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
       if (lane == 0) bulk_wait_read_all();  // this warp's previous O box has been read out
       __syncwarp();
     }
+    uint32_t ov[D / 64][32];
+    if constexpr (D == 128) {
+      tmem_ld_x32_nw(tl + C::kColO + o0, ov[0]);
+      tmem_ld_x32_nw(tl + C::kColO + o0 + 32, ov[D / 64 - 1]);
+      tmem_ld_wait2(ov[0], ov[D / 64 - 1]);
+    } else {
+      tmem_ld_x32(tl + C::kColO + o0, ov[0]);
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&bars.o_empty));  // O's columns are free for the next tile
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
-      uint32_t v[32];
-      tmem_ld_x32(tl + C::kColO + o0 + c * 32, v);
+      const uint32_t (&v)[32] = ov[c];
       uint32_t w[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e)
@@ -415,8 +424,6 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
         for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
       }
     }
-    tc_fence_before();
-    mbar_arrive(smem_u32(&bars.o_empty));
     if (staged) {
       fence_proxy_async_smem();
       __syncwarp();
