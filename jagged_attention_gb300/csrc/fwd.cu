@@ -130,26 +130,34 @@ __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const C
     for (int c = 0; c < C::kChunks; ++c)
       tma_load_2d(sQ + c * C::kChunkBytes, q_map, smem_u32(&bars.q_full), x0 + c * 64, qrow);
     ++nq;
-    for (int j = 0; j < t.cost && ok; ++j) {
+    // K runs one block ahead of V: a V load waits for the PV two blocks
+    // back, which must not hold up the K the next QK^T needs
+    auto load_k = [&](int j) -> bool {
       const uint32_t st = nk % C::kStages, ph = (nk / C::kStages) & 1;
-      const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
-      const uint32_t sV = sbase + C::kOffV + st * C::kTileBytes;
-      ok = mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, ab);
-      if (!ok) break;
+      if (!mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, ab)) return false;
       mbar_arrive_expect_tx(smem_u32(&bars.k_full[st]), C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_2d(sK + c * C::kChunkBytes, k_map, smem_u32(&bars.k_full[st]), x0 + c * 64,
-                    kv0 + j * 128);
+        tma_load_2d(sbase + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes, k_map,
+                    smem_u32(&bars.k_full[st]), x0 + c * 64, kv0 + j * 128);
       ++nk;
-      ok = mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, ab);
-      if (!ok) break;
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      const uint32_t st = nv % C::kStages, ph = (nv / C::kStages) & 1;
+      if (!mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, ab)) return false;
       mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_2d(sV + c * C::kChunkBytes, v_map, smem_u32(&bars.v_full[st]), x0 + c * 64,
-                    kv0 + j * 128);
+        tma_load_2d(sbase + C::kOffV + st * C::kTileBytes + c * C::kChunkBytes, v_map,
+                    smem_u32(&bars.v_full[st]), x0 + c * 64, kv0 + j * 128);
       ++nv;
+      return true;
+    };
+    ok = load_k(0);
+    for (int j = 0; j < t.cost && ok; ++j) {
+      if (j + 1 < t.cost) ok = load_k(j + 1);
+      if (ok) ok = load_v(j);
     }
   }
   // Let every copy this thread issued land before the CTA can exit: the last
