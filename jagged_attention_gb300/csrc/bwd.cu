@@ -353,7 +353,6 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
                              *reinterpret_cast<const uint64_t*>(lse2 + j)), p0, p1);
             p0 = fast_exp2(p0);
             p1 = fast_exp2(p1);
-            if (!kv_ok) p0 = p1 = 0.0f;
             ph[e] = pack_bf16x2(p0, p1);
           }
         } else {  // packed tile: only this key row's own sequence
@@ -393,17 +392,24 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
         } else {
           tmem_ld_x32(tl + C::kColDP + c0 + 32, v);
         }
+        // Key rows past the sequence get dS^T = 0 (it reaches dQ through K);
+        // their P^T is left unmasked, since it only reaches rows of dV and dK
+        // that are never stored.
         uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = c0 + c * 32 + 2 * e;
-          const uint32_t pp = p[c * 16 + e];
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u)),
-                           f2_sub(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
-                                  *reinterpret_cast<const uint64_t*>(dlt + j))),
-                    d0, d1);
-          w[e] = pack_bf16x2(d0, d1);
+        for (int e = 0; e < 16; ++e) w[e] = 0u;
+        if (kv_ok) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = c0 + c * 32 + 2 * e;
+            const uint32_t pp = p[c * 16 + e];
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u)),
+                             f2_sub(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                    *reinterpret_cast<const uint64_t*>(dlt + j))),
+                      d0, d1);
+            w[e] = pack_bf16x2(d0, d1);
+          }
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
