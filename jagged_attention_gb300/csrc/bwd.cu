@@ -286,7 +286,8 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
 // lane): group g (warps 4g .. 4g+3) owns query columns [64g, 64g + 64).  The
 // backward needs no row reduction (LSE and Delta are given), so the halves
 // are independent; splitting them puts two warps on every SM sub-partition,
-// which keeps the exp2 unit and the TMEM traffic busy.
+// whose instruction issue is what bounds this work (hence the packed fp32
+// pairs below).
 template <int D, bool kPack, class Seq>
 __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uint32_t tmem,
                             BwdBars& bars, const Abort& ab, Seq& seq, int g) {
