@@ -357,8 +357,8 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
             ph[e] = pack_bf16x2(p0, p1);
           }
         } else {  // packed tile: only this key row's own sequence
-#pragma unroll
           const uint64_t sl2x2 = f2_pack(a.scale_log2, a.scale_log2);
+#pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = c0 + c * 32 + 2 * e;
             float p0, p1;
