@@ -56,7 +56,7 @@ struct FwdCfg {
   // rows) at a time
   static constexpr int kOffOStg = kOffXSum + 2 * 2 * 2 * 128 * 4;
   static constexpr int kOffBar = kOffOStg + (D == 128 ? 2 * 16384 : 0);
-  static constexpr int kBarBytes = 512;
+  static constexpr int kBarBytes = 640;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + barriers + alignment slack
   static constexpr uint32_t kColS = 0;               // 2 x 128 fp32 columns
   static constexpr uint32_t kColO = 256;             // D fp32 columns
@@ -72,8 +72,11 @@ struct FwdBars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
   uint64_t o_empty;
-  uint64_t max_ready[2];  // both groups' partial row maxima of a block are in shared memory
-  uint64_t sum_ready[2];  // both groups' partial row sums of a tile are in shared memory
+  // per buffer and TMEM lane quadrant (the two warps, one per group, that
+  // share those 32 rows): both groups' partial row maxima of a block, and
+  // partial row sums of a tile, are in shared memory
+  uint64_t max_ready[2][4];
+  uint64_t sum_ready[2][4];
   uint64_t drain;
   TileRing ring;  // dynamic schedules: tile indices from the producer to the other roles
   uint32_t tmem_base;
@@ -327,8 +330,8 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
       // combine with the other group's maximum of this row
       float* xm = xmax + (gj & 1) * 256;
       xm[grp * 128 + r] = mx;
-      mbar_arrive(smem_u32(&bars.max_ready[gj & 1]));
-      if (!warp_wait(smem_u32(&bars.max_ready[gj & 1]), (gj >> 1) & 1, ab)) return;
+      mbar_arrive(smem_u32(&bars.max_ready[gj & 1][warp & 3]));
+      if (!warp_wait(smem_u32(&bars.max_ready[gj & 1][warp & 3]), (gj >> 1) & 1, ab)) return;
       mx = fmaxf(mx, xm[(grp ^ 1) * 128 + r]);
       const float m_cand = mx * sl2;
       const bool resc = m_cand > m_run + kRescaleThreshold;
@@ -387,8 +390,8 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
     float* xs = xsum + (tq & 1) * 512;  // [group][exact, rounded][128]
     xs[grp * 256 + r] = l_run;
     xs[grp * 256 + 128 + r] = lr_run;
-    mbar_arrive(smem_u32(&bars.sum_ready[tq & 1]));
-    if (!warp_wait(smem_u32(&bars.sum_ready[tq & 1]), (tq >> 1) & 1, ab)) return;
+    mbar_arrive(smem_u32(&bars.sum_ready[tq & 1][warp & 3]));
+    if (!warp_wait(smem_u32(&bars.sum_ready[tq & 1][warp & 3]), (tq >> 1) & 1, ab)) return;
     l_run += xs[(grp ^ 1) * 256 + r];
     lr_run += xs[(grp ^ 1) * 256 + 128 + r];
     const uint32_t gl = g + t.cost - 1;
@@ -473,8 +476,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_init(smem_u32(&bars.s_full[s]), 1);
       mbar_init(smem_u32(&bars.s_empty[s]), 256);
       mbar_init(smem_u32(&bars.p_full[s]), 256);
-      mbar_init(smem_u32(&bars.max_ready[s]), 256);
-      mbar_init(smem_u32(&bars.sum_ready[s]), 256);
+      for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bars.max_ready[s][q]), 64);
+      for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bars.sum_ready[s][q]), 64);
       mbar_init(smem_u32(&bars.pv_done[s]), 1);
     }
     mbar_init(smem_u32(&bars.o_empty), 256);
