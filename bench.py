@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from the committed ncu captures (profiles/), keyed by
 # kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 871.8 MB at 256 sequences, x3.730
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2515e+09, "src_hash": "1513f167c1a90db3"},
-    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 478.7 MB at 256 sequences, x3.730
-    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7854e+09, "src_hash": "a15440ac79b02af5"},
+    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 872.4 MB at 256 sequences, x3.730
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2536e+09, "src_hash": "1513f167c1a90db3"},
+    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 479.0 MB at 256 sequences, x3.730
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7866e+09, "src_hash": "e8a39f048b13c6d2"},
 }
 
 
