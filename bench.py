@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from the committed ncu captures (profiles/), keyed by
 # kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 872.4 MB at 256 sequences, x3.730
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2536e+09, "src_hash": "1513f167c1a90db3"},
-    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 479.0 MB at 256 sequences, x3.730
-    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7866e+09, "src_hash": "e8a39f048b13c6d2"},
+    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 871.9 MB at 256 sequences, x3.730
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2518e+09, "src_hash": "33ff8d09421b475d"},
+    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 478.9 MB at 256 sequences, x3.730
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7859e+09, "src_hash": "2b8238ba754f8ed8"},
 }
 
 
@@ -69,6 +69,31 @@ def flops(prob, which: str) -> float:
     return base if which == "fwd" else 2.5 * base
 
 
+def packed_runs(prob, pack: bool) -> list:
+    """Runs [b, e) of sequences the library packs into one tile: greedy runs of
+    short sequences totalling <= 128 rows with >= 2 non-empty (self mode only)."""
+    out = []
+    if not pack or prob.mode == "broadcast":
+        return out
+    klen = prob.kv_lengths
+    b = 0
+    while b < len(klen):
+        if klen[b] == 0 or klen[b] > 128:
+            b += 1
+            continue
+        total, e, nonempty = klen[b], b + 1, 1
+        while e < len(klen) and total + klen[e] <= 128:
+            total += klen[e]
+            nonempty += klen[e] > 0
+            e += 1
+        if nonempty >= 2:
+            out.append((b, e))
+            b = e
+        else:
+            b += 1
+    return out
+
+
 def dq_rows_cleared(prob, pack: bool) -> int:
     """Query rows whose fp32 dQ the backward pre-pass clears: the library clears
     the rows tiles reduce-add into or never write (all rows in broadcast mode;
@@ -79,22 +104,8 @@ def dq_rows_cleared(prob, pack: bool) -> int:
         return prob.n_q_rows
     klen, qlen = prob.kv_lengths, prob.q_lengths
     packed = np.zeros(len(klen), dtype=bool)
-    if pack:  # greedy runs of short sequences totalling <= 128 rows, >= 2 non-empty
-        b = 0
-        while b < len(klen):
-            if klen[b] == 0 or klen[b] > 128:
-                b += 1
-                continue
-            total, e, nonempty = klen[b], b + 1, 1
-            while e < len(klen) and total + klen[e] <= 128:
-                total += klen[e]
-                nonempty += klen[e] > 0
-                e += 1
-            if nonempty >= 2:
-                packed[b:e] = True
-                b = e
-            else:
-                b += 1
+    for b, e in packed_runs(prob, pack):
+        packed[b:e] = True
     runs, rows, prev_end, pos = 0, 0, -1, 0
     for b in range(len(qlen)):
         s, e = pos, pos + int(qlen[b])
@@ -107,8 +118,31 @@ def dq_rows_cleared(prob, pack: bool) -> int:
     return prob.n_q_rows if (runs > 4 or 2 * rows > prob.n_q_rows) else rows
 
 
-def alg_bytes(prob, which: str, pack: bool = False) -> float:
-    """Algorithmic HBM bytes of one launch (each tensor read or written once)."""
+def tiles_form_delta(prob, pack: bool = False, delta_prepass: bool = False,
+                     delta_in_tiles: bool = False) -> bool:
+    """Whether the backward forms Delta in its main pass, by the library's rule:
+    every sequence with queries has at most one 128-key block, and the tiles
+    hold at least 96 key rows on average (or the flags force one way)."""
+    if delta_prepass:
+        return False
+    klen, qlen = np.asarray(prob.kv_lengths), np.asarray(prob.q_lengths)
+    if not np.all((qlen == 0) | (klen <= 128)):
+        return False
+    if delta_in_tiles:
+        return True
+    runs = packed_runs(prob, pack)
+    in_run = np.zeros(len(klen), dtype=bool)
+    for b, e in runs:
+        in_run[b:e] = True
+    alone = ~in_run & (qlen > 0) & (klen > 0)
+    tiles = len(runs) + int(alone.sum())
+    rows = int(klen[in_run].sum()) + int(klen[alone].sum())
+    return tiles > 0 and rows >= 96 * tiles
+
+
+def alg_bytes(prob, which: str, pack: bool = False, own_delta: bool = False) -> float:
+    """Algorithmic HBM bytes of one launch (each tensor read or written once);
+    own_delta: Delta is formed in the main pass, so neither O nor Delta moves."""
     row = prob.H * prob.D
     q = prob.n_q_rows * row * 2
     kv = prob.k.shape[0] * row * 2
@@ -117,9 +151,9 @@ def alg_bytes(prob, which: str, pack: bool = False) -> float:
     if which == "fwd":
         return q + 2 * kv + o + lse
     if which == "pre":  # O and dO read, Delta written, the reduce-added dQ rows cleared
-        return 2 * o + lse + dq_rows_cleared(prob, pack) * row * 4
+        return (0 if own_delta else 2 * o + lse) + dq_rows_cleared(prob, pack) * row * 4
     # main: Q, K, V, dO, LSE, Delta read; dQ (fp32), dK, dV written
-    return q + 2 * kv + o + 2 * lse + prob.n_q_rows * row * 4 + 2 * kv
+    return q + 2 * kv + o + (1 if own_delta else 2) * lse + prob.n_q_rows * row * 4 + 2 * kv
 
 
 def src_hash(name: str) -> str:
@@ -306,7 +340,10 @@ def run_ours(args, rank, world, dist):
     w = workloads.WORKLOADS[args.workload]
     prob = workloads.make_workload(args.workload, seed=rank_seed(args.seed, rank), device=dev,
                                    batch=args.batch)
-    flags = (jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
+    flags = ((jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
+             | (jfa.PLAN_DELTA_PREPASS if args.delta_prepass else 0)
+             | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0))
+    own_delta = tiles_form_delta(prob, args.pack, args.delta_prepass, args.delta_in_tiles)
     plan = jfa.Plan(prob.kv_offsets, prob.q_offsets, H=prob.H, D=prob.D, Lq=prob.Lq, flags=flags)
     out = torch.empty((prob.n_o_rows, prob.H, prob.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((prob.H, prob.n_o_rows), dtype=torch.float32, device=dev)
@@ -376,15 +413,15 @@ def run_ours(args, rank, world, dist):
     per_kernel = {
         "jfa_fwd_kernel": {"ms": k_fwd / args.steps, "flops": flops(prob, "fwd"),
                            "bytes": alg_bytes(prob, "fwd"), "src": "fwd.cu"},
-        "bwd_preprocess": {"ms": k_pre / args.steps, "flops": 0.0, "bytes": alg_bytes(prob, "pre", args.pack),
-                           "src": "bwd.cu"},
+        "bwd_preprocess": {"ms": k_pre / args.steps, "flops": 0.0,
+                           "bytes": alg_bytes(prob, "pre", args.pack, own_delta), "src": "bwd.cu"},
         "jfa_bwd_kernel": {"ms": k_main / args.steps, "flops": flops(prob, "bwd"),
-                           "bytes": alg_bytes(prob, "main"), "src": "bwd.cu"},
+                           "bytes": alg_bytes(prob, "main", own_delta=own_delta), "src": "bwd.cu"},
     }
     for name, d in per_kernel.items():
         s = d["ms"] * 1e-3
         d["tflops"] = d["flops"] / s / 1e12 if d["flops"] else 0.0
-        d["gbs"] = d["bytes"] / s / 1e9
+        d["gbs"] = d["bytes"] / s / 1e9 if s > 0 else 0.0
         d["tensor_frac"] = d["tflops"] / tf_peak
         d["hbm_frac"] = d["gbs"] / bw_peak
     dom_name = max(("jfa_fwd_kernel", "jfa_bwd_kernel"), key=lambda n: per_kernel[n]["ms"])
@@ -426,7 +463,8 @@ def run_ours(args, rank, world, dist):
                    "l2": f"inputs larger than L2 (K+V {kv_gb:.2f} GB per step), no flush",
                    "parallelism": f"dp{world} (independent batches)",
                    "plan": ("short sequences packed" if args.pack else "plain schedule")
-                           + (", tiles claimed at run time" if args.dynamic else "")},
+                           + (", tiles claimed at run time" if args.dynamic else ""),
+                   "delta": "formed by the backward tiles" if own_delta else "pre-pass"},
         "fwd_tflops": per_kernel["jfa_fwd_kernel"]["tflops"],
         "bwd_tflops": flops(prob, "bwd") / ((k_pre + k_main) / args.steps * 1e-3) / 1e12,
         "pct_bf16_peak": {"fwd": 100 * per_kernel["jfa_fwd_kernel"]["tensor_frac"],
@@ -463,7 +501,9 @@ def run_e2e(args, prob, dev, stream, jfa):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * (prob.B + 1) * (
         1 if prob.q_offsets is None else 2)
     d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
-    flags = (jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
+    flags = ((jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
+             | (jfa.PLAN_DELTA_PREPASS if args.delta_prepass else 0)
+             | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0))
     s_in, s_cmp, s_out, s_plan = (torch.cuda.Stream(device=dev) for _ in range(4))
 
     def buffers():
@@ -532,6 +572,10 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--dynamic", action="store_true",
                     help="claim tiles at run time (JFA_PLAN_DYNAMIC) instead of the host deal")
+    ap.add_argument("--delta-prepass", action="store_true",
+                    help="form Delta in the pre-pass even where the backward tiles could (A/B)")
+    ap.add_argument("--delta-in-tiles", action="store_true",
+                    help="let the backward tiles form Delta wherever they can, whatever their fill")
     ap.add_argument("--pack", action="store_true",
                     help="plan with short sequences packed into shared tiles (block-diagonal fast path)")
     ap.add_argument("--batch", type=int, default=None,

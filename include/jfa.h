@@ -118,6 +118,24 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
  */
 #define JFA_PLAN_DYNAMIC 2u
 
+/*
+ * Where Delta comes from.  When every sequence that has queries has at most
+ * 128 keys (one key block: the block-diagonal and other short-sequence
+ * cases), each backward tile meets all the keys of its queries and can form
+ * Delta_i = sum_j P_ij dP_ij over them itself.  That is the same quantity as
+ * sum_d dO_id O_id, because O = P V and dP = dO V^T, so the pre-pass that
+ * reads O and dO only for Delta is skipped (the backward then does not read
+ * O at all).  The sums cost every tile the same whatever its fill, so by
+ * default the tiles form Delta only when they hold at least 96 key rows on
+ * average (full tiles, as with JFA_PLAN_PACK_SHORT on 64-token segments).
+ * JFA_PLAN_DELTA_PREPASS: always use the pre-pass.
+ * JFA_PLAN_DELTA_IN_TILES: let the tiles form Delta whenever they hold all
+ *   the keys of their queries, whatever their fill.
+ * Setting both is JFA_ERR_INVALID_ARG.
+ */
+#define JFA_PLAN_DELTA_PREPASS 4u
+#define JFA_PLAN_DELTA_IN_TILES 8u
+
 /* jfa_plan_create with flags (0 = the schedule described above). */
 int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                        int Lq, int D, int num_ctas, unsigned flags, void* stream, jfa_plan_t* out);
@@ -164,6 +182,9 @@ size_t jfa_bwd_workspace_bytes(jfa_plan_t plan);
  * forms Delta_i = sum_d dO_id O_id (the row sum the TLX Block Attention page
  * calls the "Di" preprocessing, "One Constraint, Five Eliminations"), then
  * runs the key/value-stationary pass that produces dK, dV and reduce-adds dQ.
+ * Where every tile holds all the keys of its queries, the main pass may form
+ * Delta itself instead (see JFA_PLAN_DELTA_PREPASS); the workspace is then
+ * not written, but its size and alignment rules stay the same.
  */
 int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const void* out,
             const void* dout, const float* lse, float scale, float* dq, void* dk, void* dv,
@@ -172,7 +193,8 @@ int jfa_bwd(jfa_plan_t plan, const void* q, const void* k, const void* v, const 
 /*
  * The two stages jfa_bwd runs, for callers that schedule them separately
  * (same arguments and rules as jfa_bwd).
- * jfa_bwd_preprocess: Delta (into workspace) from out and dout, clears the dq
+ * jfa_bwd_preprocess: Delta (into workspace) from out and dout -- skipped when
+ *   the main pass forms Delta itself (see JFA_PLAN_DELTA_PREPASS) --, clears the dq
  *   rows the main pass reduce-adds into or never writes (all of them in
  *   broadcast mode; with query offsets, those of sequences with no key or
  *   more than one key block -- a sequence with one key block, or in a packed
@@ -212,7 +234,9 @@ int jfa_plan_device_status(jfa_plan_t plan, void* stream, int* raw);
  * sums live in one file-scope static __device__ array of
  * JFA_NOALLOC_SCRATCH_BYTES, which every GPU that loads this library holds
  * until the process exits.  A problem whose scratch (about 4 * H * n_o bytes
- * of Delta plus 16 bytes per backward tile) does not fit is rejected with
+ * of Delta plus 16 bytes per backward tile; no Delta where the tiles form it,
+ * under the default rule given with JFA_PLAN_DELTA_PREPASS) does not fit is
+ * rejected with
  * JFA_ERR_WORKSPACE before anything is launched.  The call allocates no
  * device memory and calls no allocating library routine.
  *

@@ -30,6 +30,8 @@ STATUS_NAMES = {
 BLOCK_M = BLOCK_N = 128
 PLAN_PACK_SHORT = 1  # JFA_PLAN_PACK_SHORT
 PLAN_DYNAMIC = 2  # JFA_PLAN_DYNAMIC
+PLAN_DELTA_PREPASS = 4  # JFA_PLAN_DELTA_PREPASS
+PLAN_DELTA_IN_TILES = 8  # JFA_PLAN_DELTA_IN_TILES
 
 
 class JfaError(RuntimeError):
@@ -259,7 +261,8 @@ def header_functions() -> list[str]:
 
 
 def bwd_preprocess(plan: Plan, out, dout, dq, dk, dv, workspace, stream=None):
-    """Delta into ``workspace``, dq cleared, dK/dV of query-less sequences zeroed."""
+    """Delta into ``workspace`` (unless the plan's main pass forms it), dq cleared,
+    dK/dV of query-less sequences zeroed."""
     _check(lib().jfa_bwd_preprocess(plan.handle, _dev(out, "out", torch.bfloat16),
                                     _dev(dout, "dout", torch.bfloat16), _dev(dq, "dq", torch.float32),
                                     _dev(dk, "dk", torch.bfloat16), _dev(dv, "dv", torch.bfloat16),

@@ -108,6 +108,41 @@ int lengths_of(const int32_t* kv_off, const int32_t* q_off, int B, int Lq,
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Every sequence that has queries has at most one key block: each backward
+// tile then meets all the keys of its queries and can form Delta itself.
+bool tiles_hold_all_keys(const std::vector<int64_t>& qlen, const std::vector<int64_t>& kvlen) {
+  for (size_t b = 0; b < qlen.size(); ++b)
+    if (qlen[b] > 0 && kvlen[b] > jfa::kBN) return false;
+  return true;
+}
+
+// Mean number of key rows the backward tiles hold (a packed tile counts the
+// rows of all its sequences).
+double mean_tile_keys(const jfa::Schedule& s, const int32_t* kv_off) {
+  if (s.T == 0) return 0.0;
+  double rows = 0.0;
+  for (int t = 0; t < s.T; ++t) {
+    const int b = s.tiles[4 * t], n = s.tiles[4 * t + 2];
+    rows += n < 0 ? kv_off[b - n] - kv_off[b]
+                  : std::min<int64_t>(jfa::kBN, int64_t(kv_off[b + 1] - kv_off[b]) - int64_t(n) * jfa::kBN);
+  }
+  return rows / s.T;
+}
+
+// Whether the backward tiles form Delta.  Forming it costs every step of a
+// tile the same cross-lane sums however few key rows the tile holds, while
+// the pre-pass it replaces costs in proportion to the rows: on the GB300 it
+// paid with full tiles (64-token segments packed two per tile: step -11%)
+// and came out even with half-full ones (the same segments one per tile:
+// 15.08 against 15.05 ms), so by default tiles form it when they hold at
+// least 96 key rows on average.
+bool tiles_form_delta(unsigned flags, const std::vector<int64_t>& qlen,
+                      const std::vector<int64_t>& kvlen, const jfa::Schedule& bwd,
+                      const int32_t* kv_off) {
+  if ((flags & JFA_PLAN_DELTA_PREPASS) || !tiles_hold_all_keys(qlen, kvlen)) return false;
+  return (flags & JFA_PLAN_DELTA_IN_TILES) || mean_tile_keys(bwd, kv_off) >= 96.0;
+}
+
 // Packing needs self mode with one offsets array for queries and keys.
 bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B) {
   if (!(flags & JFA_PLAN_PACK_SHORT) || !q_off) return false;
@@ -164,6 +199,7 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
                        int Lq, int D, int num_ctas, unsigned flags, void* stream, jfa_plan_t* out) {
   if (!out || !kv_offsets_host || B < 1 || H < 1 || num_ctas < 0) return JFA_ERR_INVALID_ARG;
   *out = nullptr;
+  if ((flags & JFA_PLAN_DELTA_PREPASS) && (flags & JFA_PLAN_DELTA_IN_TILES)) return JFA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
   std::vector<int64_t> qlen, kvlen;
   int64_t n_kv = 0, n_q = 0;
@@ -222,6 +258,7 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   p->dynamic = (flags & JFA_PLAN_DYNAMIC) != 0;
   p->fwd = jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->dynamic);
   p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->dynamic);
+  p->own_delta = tiles_form_delta(flags, qlen, kvlen, p->bwd, kv_offsets_host);
   for (int b = 0; b < B; ++b) {
     if (qlen[b] == 0 && kvlen[b] > 0) {
       const int64_t s = kv_offsets_host[b], e = kv_offsets_host[b + 1];
@@ -374,7 +411,7 @@ int jfa_bwd_preprocess(jfa_plan_t plan, const void* out, const void* dout, float
         cudaMemsetAsync(static_cast<uint8_t*>(dv) + off, 0, len, s) != cudaSuccess)
       return JFA_ERR_CUDA;
   }
-  if (plan->bwd.P == 0 || plan->n_o == 0) return JFA_OK;
+  if (plan->bwd.P == 0 || plan->n_o == 0 || plan->own_delta) return JFA_OK;
   cudaError_t e = jfa::launch_delta(static_cast<const uint16_t*>(out),
                                     static_cast<const uint16_t*>(dout),
                                     static_cast<float*>(workspace), plan->n_o, plan->H, plan->D, s);
@@ -415,6 +452,7 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
   a.status = plan->d_status;
   a.packed = plan->packed;
   a.own_rows = plan->dq_own_rows;
+  a.own_delta = plan->own_delta;
   a.T = plan->bwd.T;
   if (plan->dynamic) {
     a.dyn_counter = plan->d_counters + 1;
@@ -505,7 +543,8 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   const size_t o_t = align_up(o_q + (q_offsets_host ? (B + 1) * 4 : 0), 256);
   const size_t o_p = align_up(o_t + sched.tiles.size() * 4, 256);
   const size_t o_d = align_up(o_p + sched.cta_ptr.size() * 4, 256);
-  const size_t need = o_d + static_cast<size_t>(n_o) * H * sizeof(float);
+  const bool own_delta = tiles_form_delta(0u, qlen, kvlen, sched, kv_offsets_host);  // no Delta scratch
+  const size_t need = o_d + (own_delta ? 0 : static_cast<size_t>(n_o) * H * sizeof(float));
   if (need > JFA_NOALLOC_SCRATCH_BYTES) return JFA_ERR_WORKSPACE;
 
   uint8_t* scratch = nullptr;
@@ -514,7 +553,7 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // every byte before Delta is rewritten by this call (the status word
-  // starts at 0); Delta is written in full by the pre-pass below
+  // starts at 0); Delta, where there is a pre-pass, is written in full by it
   std::vector<uint8_t> host(o_d, 0);
   std::memcpy(&host[o_kv], kv_offsets_host, (B + 1) * 4);
   if (q_offsets_host) std::memcpy(&host[o_q], q_offsets_host, (B + 1) * 4);
@@ -537,10 +576,13 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
     }
   }
   if (sched.P == 0 || n_o == 0) return JFA_OK;
-  float* delta = reinterpret_cast<float*>(scratch + o_d);
-  cudaError_t e = jfa::launch_delta(static_cast<const uint16_t*>(out),
-                                    static_cast<const uint16_t*>(dout), delta, n_o, H, D, s);
-  if (e != cudaSuccess) return JFA_ERR_CUDA;
+  float* delta = own_delta ? nullptr : reinterpret_cast<float*>(scratch + o_d);
+  cudaError_t e = cudaSuccess;
+  if (!own_delta) {
+    e = jfa::launch_delta(static_cast<const uint16_t*>(out), static_cast<const uint16_t*>(dout),
+                          delta, n_o, H, D, s);
+    if (e != cudaSuccess) return JFA_ERR_CUDA;
+  }
   CUtensorMap qm, km, vm, dom, dqm, dkm, dvm;
   if (make_map(&qm, q, n_q, cols) || make_map(&km, k, n_kv, cols) || make_map(&vm, v, n_kv, cols) ||
       make_map(&dom, dout, n_o, cols) || make_map_dq(&dqm, dq, n_q, cols) ||
@@ -567,6 +609,7 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   a.dv = static_cast<uint16_t*>(dv);
   a.status = device_status ? device_status : reinterpret_cast<int*>(scratch + o_st);
   a.packed = false;
+  a.own_delta = own_delta;
   e = jfa::launch_bwd(a, qm, km, vm, dom, dqm, dkm, dvm, sched.P, s);
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }

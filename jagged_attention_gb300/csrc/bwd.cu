@@ -105,6 +105,7 @@ struct BwdBars {
   uint64_t dq_full, dq_empty;
   uint64_t dkv_full, dkv_empty;
   uint64_t lse_ready[2], lse_done[2];  // per softmax group: LSE / Delta staging
+  uint64_t dsum_part[2], dsum_ready[2];  // per softmax group: Delta formed in the kernel
   uint64_t drain;
   TileRing ring;  // dynamic schedules: tile indices from the producer to the other roles
   uint32_t tmem_base;
@@ -282,15 +283,34 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
 }
 
 // ---------------------------------------------------------------------------
+// One step of a sum across the warp's lanes of 2N values per lane: lanes with
+// bit N clear keep values [0, N), the others [N, 2N), and each adds its
+// partner's copy of the half it keeps.  After the steps N = 16, 8, 4, 2, 1 on
+// 32 values, x[0] of lane l is the sum over all lanes of value l (a fixed
+// order of additions, so the result is deterministic).
+template <int N>
+__device__ __forceinline__ void lane_fold(float (&x)[32], int lane) {
+  const bool hi = (lane & N) != 0;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const float send = hi ? x[k] : x[k + N];
+    const float keep = hi ? x[k + N] : x[k];
+    x[k] = keep + __shfl_xor_sync(0xffffffffu, send, N);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Softmax groups: P^T and dS^T.  Two warpgroups share every key row (TMEM
 // lane): group g (warps 4g .. 4g+3) owns query columns [64g, 64g + 64).  The
 // backward needs no row reduction (LSE and Delta are given), so the halves
 // are independent; splitting them puts two warps on every SM sub-partition,
 // whose instruction issue is what bounds this work (hence the packed fp32
-// pairs below).
-template <int D, bool kPack, class Seq>
-__device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uint32_t tmem,
-                            BwdBars& bars, const Abort& ab, Seq& seq, int g) {
+// pairs below).  kOwnDelta: the tiles form Delta themselves (a separate copy
+// of the loop, so the common case carries none of that code).
+template <int D, bool kPack, bool kOwnDelta, class Seq>
+__device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem, uint32_t sbase,
+                                                 uint32_t tmem, BwdBars& bars, const Abort& ab,
+                                                 Seq& seq, int g) {
   using C = BwdCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;  // key row of the tile = TMEM lane
@@ -330,7 +350,7 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
         const bool q_ok = q < qlen;
         const int64_t idx = int64_t(t.h) * a.pb.n_o + o_base + q;
         lse2[c0 + r] = q_ok ? -(a.lse[idx] * 1.4426950408889634f) : -INFINITY;  // -LSE, log2 units
-        dlt[c0 + r] = q_ok ? a.delta[idx] : 0.0f;
+        if constexpr (!kOwnDelta) dlt[c0 + r] = q_ok ? a.delta[idx] : 0.0f;
       }
       mbar_arrive(lse_ready);
       if (!warp_wait_b(lse_ready, gm & 1, ab)) return;
@@ -381,6 +401,49 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
       // the dS^T buffer is free once the previous step's dK and dQ products completed
       if (!warp_wait_b(smem_u32(&bars.ds_empty), (gm & 1) ^ 1, ab)) return;
       tc_fence_after();
+      if constexpr (kOwnDelta) {
+        // The tile holds every key its queries meet, so Delta_i = sum_d dO_id
+        // O_id equals sum_j P_ij dP_ij over the tile's key rows (O = P V and
+        // dP = dO V^T).  Each warp sums its 32 key rows across lanes, the four
+        // warps' sums meet in the first kilobyte of this group's dS^T chunk
+        // (free since ds_empty; overwritten by dS^T only after dsum_ready),
+        // and 64 threads add them in a fixed order.
+        float* part = reinterpret_cast<float*>(smem + C::kOffDS + g * C::kChunkBytes);
+        uint32_t pq[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          if (c == 0) {
+            tmem_ld_x32_nw(tl + C::kColS + c0, pq);
+            tmem_ld_x32_nw(tl + C::kColDP + c0, v);
+            tmem_ld_wait2(pq, v);
+          } else {
+            tmem_ld_x32(tl + C::kColDP + c0 + 32, v);
+          }
+          float x[32];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint32_t pp = pq[c * 16 + e];
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u)),
+                             f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]))),
+                      x0, x1);
+            x[2 * e] = kv_ok ? x0 : 0.0f;  // key rows past the sequence hold another's P^T
+            x[2 * e + 1] = kv_ok ? x1 : 0.0f;
+          }
+          lane_fold<16>(x, lane);
+          lane_fold<8>(x, lane);
+          lane_fold<4>(x, lane);
+          lane_fold<2>(x, lane);
+          lane_fold<1>(x, lane);
+          part[(warp & 3) * 64 + c * 32 + lane] = x[0];
+        }
+        mbar_arrive(smem_u32(&bars.dsum_part[g]));
+        if (!warp_wait_b(smem_u32(&bars.dsum_part[g]), gm & 1, ab)) return;
+        if (r < 64) dlt[c0 + r] = (part[r] + part[64 + r]) + (part[128 + r] + part[192 + r]);
+        mbar_arrive(smem_u32(&bars.dsum_ready[g]));
+        if (!warp_wait_b(smem_u32(&bars.dsum_ready[g]), gm & 1, ab)) return;
+      }
       const uint32_t sDS = sbase + C::kOffDS + g * C::kChunkBytes;  // 128-byte chunk g of each row
       uint32_t p[32];  // P^T of this row, back from TMEM
 #pragma unroll
@@ -423,6 +486,15 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
       mbar_arrive(lse_done);  // this block's LSE / Delta no longer read by this thread
     }
   }
+}
+
+template <int D, bool kPack, class Seq>
+__device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uint32_t tmem,
+                            BwdBars& bars, const Abort& ab, Seq& seq, int g) {
+  if (a.own_delta)
+    bwd_softmax_loop<D, kPack, true>(a, smem, sbase, tmem, bars, ab, seq, g);
+  else
+    bwd_softmax_loop<D, kPack, false>(a, smem, sbase, tmem, bars, ab, seq, g);
 }
 
 // ---------------------------------------------------------------------------
@@ -654,6 +726,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     for (int g = 0; g < 2; ++g) {
       mbar_init(smem_u32(&bars.lse_ready[g]), 128);
       mbar_init(smem_u32(&bars.lse_done[g]), 128);
+      mbar_init(smem_u32(&bars.dsum_part[g]), 128);
+      mbar_init(smem_u32(&bars.dsum_ready[g]), 128);
     }
     mbar_init(smem_u32(&bars.drain), 1);
     bars.abort_flag = 0;

@@ -44,6 +44,8 @@ struct BwdArgs {
   bool packed;             // the schedule may hold packed tiles {b0, h, -nseq, 1}
   bool own_rows = false;   // the pre-pass left the dQ rows of single-key-block
                            // sequences uncleared: their one tile stores them
+  bool own_delta = false;  // every tile holds all the keys its queries meet: the
+                           // kernel forms Delta itself and `delta` is not read
   int* dyn_counter = nullptr;  // dynamic schedule: claim counter (zeroed before the launch)
   int T = 0;                   // tiles in the schedule
 };

@@ -58,6 +58,10 @@ struct jfa_plan {
   std::vector<std::pair<int64_t, int64_t>> dq_rows_to_clear;
   bool dq_own_rows = false;  // some rows are left to the tiles that own them
   bool dynamic = false;      // tiles claimed at run time (JFA_PLAN_DYNAMIC)
+  // every sequence with queries has at most one key block, so each backward
+  // tile meets all the keys of its queries and forms Delta itself: the
+  // pre-pass skips the Delta kernel (unless JFA_PLAN_DELTA_PREPASS)
+  bool own_delta = false;
   int* d_counters = nullptr; // dynamic: claim counters [fwd, bwd]
   int device = 0;
   int num_ctas = 0;

@@ -25,6 +25,16 @@ def test_exports_every_declared_function():
         assert hasattr(L, n), n
 
 
+def test_binding_constants_match_the_header():
+    import re
+    text = jfa.HEADER.read_text()
+    flags = {m[0]: int(m[1]) for m in re.findall(r"#define JFA_PLAN_(\w+) (\d+)u", text)}
+    assert flags == {"PACK_SHORT": jfa.PLAN_PACK_SHORT, "DYNAMIC": jfa.PLAN_DYNAMIC,
+                     "DELTA_PREPASS": jfa.PLAN_DELTA_PREPASS, "DELTA_IN_TILES": jfa.PLAN_DELTA_IN_TILES}
+    codes = {int(m[1]): m[0] for m in re.findall(r"\b(JFA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text)}
+    assert codes == jfa.STATUS_NAMES
+
+
 def _ref(qlen, klen, H, P, direction, pack=None, dynamic=False):
     fn = ref_tiles.fwd_tiles if direction == 0 else ref_tiles.bwd_tiles
     return fn(qlen, klen, H, 128, 128, P, pack, dynamic)
@@ -136,14 +146,14 @@ def test_seed0_tile_counts():
         assert jfa.build_tiles(kv, qo, H=w.H, Lq=w.Lq, num_ctas=152, direction=1)[0].shape[0] == tb
 
 
-def _create(kv, qo, B, H, Lq, D, num_ctas=0):
+def _create(kv, qo, B, H, Lq, D, num_ctas=0, flags=0):
     L = jfa.lib()
     h = ctypes.c_void_p()
     kvp = None if kv is None else np.ascontiguousarray(kv, dtype=np.int32)
     qop = None if qo is None else np.ascontiguousarray(qo, dtype=np.int32)
-    rc = L.jfa_plan_create(None if kvp is None else kvp.ctypes.data_as(jfa._i32p),
-                           None if qop is None else qop.ctypes.data_as(jfa._i32p),
-                           B, H, Lq, D, num_ctas, None, ctypes.byref(h))
+    rc = L.jfa_plan_create_ex(None if kvp is None else kvp.ctypes.data_as(jfa._i32p),
+                              None if qop is None else qop.ctypes.data_as(jfa._i32p),
+                              B, H, Lq, D, num_ctas, flags, None, ctypes.byref(h))
     return rc
 
 
@@ -157,6 +167,8 @@ def test_rejects_bad_arguments_before_touching_the_device():
     assert _create([0, 5, 3], None, 2, 1, 4, 128) == 3               # decreasing
     assert _create(ok, [0, 2, 1], 2, 1, 0, 128) == 3                 # bad query offsets
     assert _create(ok, None, 2, 1, -1, 128) == 1                     # negative Lq
+    assert _create(ok, None, 2, 1, 4, 128,                           # Delta both ways
+                   flags=jfa.PLAN_DELTA_PREPASS | jfa.PLAN_DELTA_IN_TILES) == 1
     L = jfa.lib()
     T, P = ctypes.c_int(), ctypes.c_int()
     kv = np.array([0, 4, 2], dtype=np.int32)

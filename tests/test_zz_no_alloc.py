@@ -75,15 +75,39 @@ def test_noalloc_matches_jfa_bwd_twice_in_a_row(name):
             assert parity.rel_l2(g, r) <= parity.TOL_GRAD
 
 
+def test_noalloc_needs_no_delta_scratch_when_full_tiles_form_it():
+    jfa.build()
+    fn = _entry()
+    # 2^19 rows x 16 heads of Delta would fill the whole 32 MiB array, but with
+    # 128-token sequences every tile is full and forms its own Delta, so only
+    # the schedule and offsets need room
+    p = parity.to_cuda(workloads.make_problem(4096, 16, 64, "self", [128] * 4096, seed=34,
+                                              device="cuda"))
+    plan = parity.make_plan(p)
+    out, lse, _ = parity.gpu_fwd(p, plan)
+    ref = parity.gpu_bwd(p, out, lse, plan)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _call(fn, p, out, lse, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for g, r in zip(got, ref):  # compared on the device: 2^19 x 16 x 64 values each
+        assert torch.isfinite(g).all()
+        assert ((g.float() - r.float()).norm() / r.float().norm()).item() <= 1e-6
+    del p, plan, out, lse, ref, got
+    torch.cuda.empty_cache()
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     jfa.build()
     fn = _entry()
     # 2^20 broadcast rows x 16 heads of Delta (64 MiB) cannot fit the 32 MiB
     # array: the call must refuse before launching anything (tiny real buffers
-    # stand in for the tensors it never touches)
+    # stand in for the tensors it never touches).  The sequence has 129 keys,
+    # two key blocks, so Delta needs the scratch (with one key block the tiles
+    # would form it and the call would go ahead).
     t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
     f = torch.zeros(16, dtype=torch.float32, device="cuda")
-    kv = jfa._offsets([0, 1])
+    kv = jfa._offsets([0, 129])
     rc = fn(jfa._i32ptr(kv), None, 1, 16, 1 << 20, 64, t.data_ptr(), t.data_ptr(), t.data_ptr(),
             t.data_ptr(), t.data_ptr(), f.data_ptr(), 0.125, f.data_ptr(), t.data_ptr(),
             t.data_ptr(), None, torch.cuda.current_stream().cuda_stream)
