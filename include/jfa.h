@@ -164,6 +164,16 @@ int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
                     int32_t* cta_ptr_out, int* T, int* P);
 
 /*
+ * Host-only (no GPU needed): *in_tiles = 1 when a plan created from these
+ * offsets and flags has its backward tiles form Delta (the rule given with
+ * JFA_PLAN_DELTA_PREPASS), 0 when the pre-pass forms it.  With 1, jfa_bwd
+ * does not read `out`; jfa_bwd_noalloc follows the flags-0 answer.  Errors as
+ * jfa_plan_create_ex (offsets, conflicting Delta flags).
+ */
+int jfa_delta_in_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B,
+                       int Lq, unsigned flags, int* in_tiles);
+
+/*
  * Forward: out = softmax(scale Q K^T) V per sequence and head, lse as above.
  * q, k, v, out: bf16 device tensors in the layouts above; lse: fp32 device.
  * Rows of sequences without keys get O = 0 and LSE = -inf.

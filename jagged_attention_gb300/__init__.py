@@ -79,12 +79,13 @@ def lib() -> ctypes.CDLL:
             L.jfa_bwd_preprocess.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
             L.jfa_bwd_main.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
                                        _vp, ctypes.c_size_t, _vp]
+            L.jfa_delta_in_tiles.argtypes = [_i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_uint, _ip]
             L.jfa_plan_device_status.argtypes = [_vp, _vp, _ip]
             L.jfa_status_string.argtypes = [ctypes.c_int]
             L.jfa_status_string.restype = ctypes.c_char_p
             for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
                          "jfa_fwd", "jfa_bwd", "jfa_bwd_preprocess", "jfa_bwd_main",
-                         "jfa_plan_device_status"):
+                         "jfa_plan_device_status", "jfa_delta_in_tiles"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -144,6 +145,17 @@ def build_tiles(kv_offsets, q_offsets=None, *, H: int, Lq: int = 0, num_ctas: in
                              tiles.ctypes.data_as(_i32p), ptr.ctypes.data_as(_i32p),
                              ctypes.byref(T), ctypes.byref(P)), "jfa_build_tiles")
     return tiles, ptr
+
+
+def delta_in_tiles(kv_offsets, q_offsets=None, *, Lq: int = 0, flags: int = 0) -> bool:
+    """Host-only (no GPU): whether a plan with these offsets and flags has its
+    backward tiles form Delta (then the backward does not read ``out``)."""
+    kv = _offsets(kv_offsets)
+    qo = _offsets(q_offsets)
+    res = ctypes.c_int()
+    _check(lib().jfa_delta_in_tiles(_i32ptr(kv), _i32ptr(qo), kv.size - 1, Lq, flags,
+                                    ctypes.byref(res)), "jfa_delta_in_tiles")
+    return bool(res.value)
 
 
 class Plan:

@@ -190,6 +190,23 @@ int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
   return JFA_OK;
 }
 
+int jfa_delta_in_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B,
+                       int Lq, unsigned flags, int* in_tiles) {
+  if (!kv_offsets_host || B < 1 || !in_tiles) return JFA_ERR_INVALID_ARG;
+  if ((flags & JFA_PLAN_DELTA_PREPASS) && (flags & JFA_PLAN_DELTA_IN_TILES)) return JFA_ERR_INVALID_ARG;
+  std::vector<int64_t> qlen, kvlen;
+  int64_t n_kv = 0, n_q = 0;
+  int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
+  if (rc != JFA_OK) return rc;
+  std::vector<int> pack;
+  const bool packing = use_packing(flags, kv_offsets_host, q_offsets_host, B);
+  if (packing) pack = jfa::short_packs(kvlen);
+  // the mean tile fill does not depend on the head count or the CTA count
+  const Schedule s = jfa::build_bwd_schedule(qlen, kvlen, 1, 1, packing ? &pack : nullptr, false);
+  *in_tiles = tiles_form_delta(flags, qlen, kvlen, s, kv_offsets_host) ? 1 : 0;
+  return JFA_OK;
+}
+
 int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                     int Lq, int D, int num_ctas, void* stream, jfa_plan_t* out) {
   return jfa_plan_create_ex(kv_offsets_host, q_offsets_host, B, H, Lq, D, num_ctas, 0u, stream, out);

@@ -181,3 +181,63 @@ def test_rejects_bad_arguments_before_touching_the_device():
     assert L.jfa_bwd(None, None, None, None, None, None, None, 1.0, None, None, None, None, 0,
                      None) == 1
     assert L.jfa_status_string(7) == b"device wait timed out"
+
+
+def _rule(klen, qlen, pack):
+    """The documented rule, restated from the lengths alone: every sequence with
+    queries has at most 128 keys, and the backward tiles (one per such
+    sequence, or one per packed run) hold at least 96 key rows on average."""
+    klen, qlen = np.asarray(klen), np.asarray(qlen)
+    if not np.all((qlen == 0) | (klen <= 128)):
+        return False
+    runs = ref_tiles.short_packs(klen) if pack else None
+    rows = tiles = 0
+    b = 0
+    while b < len(klen):
+        n = runs[b] if runs is not None and runs[b] > 1 else 1
+        if n > 1:
+            rows, tiles, b = rows + int(klen[b:b + n].sum()), tiles + 1, b + n
+            continue
+        if qlen[b] > 0 and klen[b] > 0:
+            rows, tiles = rows + int(klen[b]), tiles + 1
+        b += 1
+    return tiles > 0 and rows >= 96 * tiles
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_delta_path_follows_the_documented_rule(seed):
+    rng = np.random.default_rng(seed)
+    for _ in range(40):
+        B = int(rng.integers(1, 30))
+        hi = int(rng.choice([64, 128, 129, 300]))
+        klen = rng.integers(0, hi + 1, B)
+        kv = np.concatenate([[0], np.cumsum(klen)]).astype(np.int32)
+        for pack in (False, True):
+            flags = jfa.PLAN_PACK_SHORT if pack else 0
+            want = _rule(klen, klen, pack)
+            assert jfa.delta_in_tiles(kv, kv, flags=flags) == want
+            assert jfa.delta_in_tiles(kv, kv, flags=flags | jfa.PLAN_DELTA_PREPASS) is False
+            assert jfa.delta_in_tiles(kv, kv, flags=flags | jfa.PLAN_DELTA_IN_TILES) == bool(np.all(klen <= 128))
+        # broadcast: every sequence has the Lq queries
+        assert jfa.delta_in_tiles(kv, None, Lq=200) == _rule(klen, np.full(B, 200), False)
+
+
+def test_delta_path_on_the_workloads():
+    # the library, the benchmark's byte accounting and the expected answer
+    # agree on every workload (lengths only: no tensors are drawn)
+    import types
+    import bench
+    cases = {("tiny_broadcast", False): False, ("jagged_self", False): False,
+             ("gem_broadcast", False): False, ("block_diag", False): False,
+             ("block_diag", True): True}
+    for (name, pack), want in cases.items():
+        w = workloads.WORKLOADS[name]
+        klen = workloads.draw_lengths(w.lengths, w.B, 0)
+        kv = workloads.offsets_from_lengths(klen)
+        qlen = np.full(w.B, w.Lq) if w.mode == "broadcast" else klen
+        qo = None if w.mode == "broadcast" else kv
+        got = jfa.delta_in_tiles(kv, qo, Lq=w.Lq, flags=jfa.PLAN_PACK_SHORT if pack else 0)
+        prob = types.SimpleNamespace(kv_lengths=klen, q_lengths=qlen, mode=w.mode)
+        assert got == want == bench.tiles_form_delta(prob, pack), name
+    with pytest.raises(jfa.JfaError):
+        jfa.delta_in_tiles([0, 5], None, Lq=4, flags=jfa.PLAN_DELTA_PREPASS | jfa.PLAN_DELTA_IN_TILES)

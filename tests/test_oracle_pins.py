@@ -9,7 +9,8 @@
   keys give O = mean(V) and LSE = scale q.k + ln L;
 * invariants: rows of P sum to one, sum_j dV_j = sum_i dO_i, sum_j dK_j = 0,
   broadcast dQ equals the sum of per-sequence self-mode dQs, block-diagonal
-  offsets equal independent per-block attention.
+  offsets equal independent per-block attention, and the row sum
+  sum_d dO_id O_id equals sum_j P_ij dP_ij (O = P V, dP = dO V^T).
 """
 import math
 
@@ -161,6 +162,23 @@ def test_gradient_invariants():
         s, e = int(off[b]), int(off[b + 1])
         assert (dv[s:e].sum(0) - g[s:e].sum(0)).abs().max() < 1e-12   # sum_j dV_j = sum_i dO_i
         assert dk[s:e].sum(0).abs().max() < 1e-12                    # sum_j dK_j = 0
+
+
+def test_row_sum_equals_p_times_dp():
+    # rowsum(dO * O) over the oracle's O equals sum_j P_ij (dO V^T)_ij with P
+    # rebuilt from the oracle's LSE: the identity that lets a backward tile
+    # holding every key of its queries form the row sum without reading O
+    # (and a check that the oracle's O and LSE describe the same P)
+    g = torch.Generator().manual_seed(12)
+    for nq, nk, D in ((7, 5, 8), (1, 1, 4), (33, 70, 16), (4, 128, 64)):
+        q, dout = (torch.randn(nq, D, generator=g, dtype=torch.float64) for _ in range(2))
+        k, v = (torch.randn(nk, D, generator=g, dtype=torch.float64) for _ in range(2))
+        scale = 1.0 / math.sqrt(D)
+        O, L = ORC.seq_fwd(q, k, v, scale)
+        P = torch.exp(scale * (q @ k.T) - L[:, None])
+        lhs = (dout * O).sum(1)
+        rhs = (P * (dout @ v.T)).sum(1)
+        assert torch.allclose(lhs, rhs, rtol=1e-12, atol=1e-12), (nq, nk, D)
 
 
 def test_broadcast_equals_sum_of_self_mode():
