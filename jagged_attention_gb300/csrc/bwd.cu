@@ -301,12 +301,13 @@ __device__ __forceinline__ void lane_fold(float (&x)[32], int lane) {
 
 // ---------------------------------------------------------------------------
 // Softmax groups: P^T and dS^T.  Two warpgroups share every key row (TMEM
-// lane): group g (warps 4g .. 4g+3) owns query columns [64g, 64g + 64).  The
-// backward needs no row reduction (LSE and Delta are given), so the halves
-// are independent; splitting them puts two warps on every SM sub-partition,
-// whose instruction issue is what bounds this work (hence the packed fp32
-// pairs below).  kOwnDelta: the tiles form Delta themselves (a separate copy
-// of the loop, so the common case carries none of that code).
+// lane): group g (warps 4g .. 4g+3) owns query columns [64g, 64g + 64).  With
+// LSE and Delta given, the backward needs no reduction along a key row, so
+// the halves are independent; splitting them puts two warps on every SM
+// sub-partition, whose instruction issue is what bounds this work (hence the
+// packed fp32 pairs below).  kOwnDelta: the tiles form Delta themselves, a
+// sum down each query column within the group (a separate copy of the loop,
+// so the common case carries none of that code).
 template <int D, bool kPack, bool kOwnDelta, class Seq>
 __device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem, uint32_t sbase,
                                                  uint32_t tmem, BwdBars& bars, const Abort& ab,
