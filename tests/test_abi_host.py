@@ -241,3 +241,18 @@ def test_delta_path_on_the_workloads():
         assert got == want == bench.tiles_form_delta(prob, pack), name
     with pytest.raises(jfa.JfaError):
         jfa.delta_in_tiles([0, 5], None, Lq=4, flags=jfa.PLAN_DELTA_PREPASS | jfa.PLAN_DELTA_IN_TILES)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bench_packing_matches_the_reference_packer(seed):
+    # bench.py counts bytes with its own copy of the packing rule
+    import types
+    import bench
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(50):
+        klen = rng.integers(0, int(rng.choice([40, 80, 140])), int(rng.integers(1, 40)))
+        prob = types.SimpleNamespace(kv_lengths=klen, q_lengths=klen, mode="self")
+        pack = ref_tiles.short_packs(klen)
+        want = [(b, b + n) for b, n in enumerate(pack) if n > 1]
+        assert bench.packed_runs(prob, True) == want
+        assert bench.packed_runs(prob, False) == []
