@@ -277,6 +277,45 @@ int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
  */
 int jfa_selftest_wait_timeout(unsigned limit_us, unsigned long long* waited_ns, void* stream);
 
+/*
+ * Plan-free forward and backward: the tensors, the host offsets and the sizes
+ * in one call, as a framework op calls attention, with no plan handle and no
+ * workspace.  Arguments mean what they mean for jfa_plan_create (kv_offsets
+ * and q_offsets on the host, q_offsets NULL for broadcast mode with Lq query
+ * rows), jfa_fwd and jfa_bwd (device tensors in the same layouts, 16-byte
+ * aligned; dq fp32, overwritten).
+ *
+ * The library keeps a plan for each distinct (device, B, H, Lq, D, offsets)
+ * it has seen, up to 8, releasing the least recently used one when a ninth
+ * arrives; each cached plan owns the backward's workspace.  The first call
+ * with new offsets builds the plan (host schedule, one device allocation and
+ * an upload synchronised on `stream`), the first backward allocates the
+ * workspace; later calls with the same offsets allocate nothing and are
+ * asynchronous.  Releasing a plan frees device memory, which synchronises the
+ * device.  Calls are serialised by a lock; backward calls with the same
+ * offsets that overlap on the GPU (different streams, no ordering) share the
+ * workspace and race: order them.
+ *
+ * Errors: the plan-creation codes (checked before any CUDA call where they
+ * need no device), then those of jfa_fwd / jfa_bwd.  A wait that ran out is
+ * recorded in the cached plan; jfa_simple_device_status reports it.
+ */
+int jfa_fwd_simple(const void* q, const void* k, const void* v, const int32_t* kv_offsets_host,
+                   const int32_t* q_offsets_host, int B, int H, int Lq, int D, float scale,
+                   void* out, float* lse, void* stream);
+int jfa_bwd_simple(const void* q, const void* k, const void* v, const int32_t* kv_offsets_host,
+                   const int32_t* q_offsets_host, int B, int H, int Lq, int D, float scale,
+                   const void* out, const void* dout, const float* lse, float* dq, void* dk,
+                   void* dv, void* stream);
+
+/* Device status of every cached plan (synchronises `stream`, then clears the
+ * words): JFA_ERR_DEVICE_TIMEOUT when any recorded a wait that ran out;
+ * *raw (optional) receives the words or-ed together. */
+int jfa_simple_device_status(void* stream, int* raw);
+
+/* Release every cached plan and workspace (synchronises the device). */
+int jfa_simple_release(void);
+
 /* Human-readable text of a status code (static storage). */
 const char* jfa_status_string(int status);
 

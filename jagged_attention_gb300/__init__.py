@@ -80,12 +80,20 @@ def lib() -> ctypes.CDLL:
             L.jfa_bwd_main.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
                                        _vp, ctypes.c_size_t, _vp]
             L.jfa_delta_in_tiles.argtypes = [_i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_uint, _ip]
+            _ci = ctypes.c_int
+            L.jfa_fwd_simple.argtypes = [_vp, _vp, _vp, _i32p, _i32p, _ci, _ci, _ci, _ci, ctypes.c_float,
+                                         _vp, _vp, _vp]
+            L.jfa_bwd_simple.argtypes = [_vp, _vp, _vp, _i32p, _i32p, _ci, _ci, _ci, _ci, ctypes.c_float,
+                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+            L.jfa_simple_device_status.argtypes = [_vp, _ip]
+            L.jfa_simple_release.argtypes = []
             L.jfa_plan_device_status.argtypes = [_vp, _vp, _ip]
             L.jfa_status_string.argtypes = [ctypes.c_int]
             L.jfa_status_string.restype = ctypes.c_char_p
             for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
                          "jfa_fwd", "jfa_bwd", "jfa_bwd_preprocess", "jfa_bwd_main",
-                         "jfa_plan_device_status", "jfa_delta_in_tiles"):
+                         "jfa_plan_device_status", "jfa_delta_in_tiles", "jfa_fwd_simple",
+                         "jfa_bwd_simple", "jfa_simple_device_status", "jfa_simple_release"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -262,6 +270,62 @@ def bwd(plan: Plan, q, k, v, out, dout, lse, scale: float, dq=None, dk=None, dv=
                          _dev(dv, "dv", torch.bfloat16), workspace.data_ptr(),
                          workspace.numel() * workspace.element_size(), _stream(stream)), "jfa_bwd")
     return dq, dk, dv
+
+
+def _simple_sizes(q, k, kv_offsets, q_offsets):
+    kv = _offsets(kv_offsets)
+    qo = _offsets(q_offsets)
+    B = kv.size - 1
+    H, D = int(k.shape[1]), int(k.shape[2])
+    Lq = int(q.shape[0]) if qo is None else 0
+    n_o = B * Lq if qo is None else int(qo[-1])
+    return kv, qo, B, H, Lq, D, n_o
+
+
+def fwd_simple(q, k, v, kv_offsets, q_offsets=None, *, scale: float, out=None, lse=None,
+               stream=None):
+    """O and LSE through jfa_fwd_simple: no plan object (the library caches one per
+    distinct offsets).  q_offsets None: broadcast mode, q holds the Lq shared rows."""
+    kv, qo, B, H, Lq, D, n_o = _simple_sizes(q, k, kv_offsets, q_offsets)
+    if out is None:
+        out = torch.empty((n_o, H, D), dtype=torch.bfloat16, device=k.device)
+    if lse is None:
+        lse = torch.empty((H, n_o), dtype=torch.float32, device=k.device)
+    _check(lib().jfa_fwd_simple(_dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16),
+                                _dev(v, "v", torch.bfloat16), _i32ptr(kv), _i32ptr(qo), B, H, Lq, D,
+                                float(scale), _dev(out, "out", torch.bfloat16),
+                                _dev(lse, "lse", torch.float32), _stream(stream)), "jfa_fwd_simple")
+    return out, lse
+
+
+def bwd_simple(q, k, v, out, dout, lse, kv_offsets, q_offsets=None, *, scale: float, dq=None,
+               dk=None, dv=None, stream=None):
+    """dQ (fp32), dK, dV through jfa_bwd_simple (cached plan and workspace)."""
+    kv, qo, B, H, Lq, D, _ = _simple_sizes(q, k, kv_offsets, q_offsets)
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    _check(lib().jfa_bwd_simple(_dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16),
+                                _dev(v, "v", torch.bfloat16), _i32ptr(kv), _i32ptr(qo), B, H, Lq, D,
+                                float(scale), _dev(out, "out", torch.bfloat16),
+                                _dev(dout, "dout", torch.bfloat16), _dev(lse, "lse", torch.float32),
+                                _dev(dq, "dq", torch.float32), _dev(dk, "dk", torch.bfloat16),
+                                _dev(dv, "dv", torch.bfloat16), _stream(stream)), "jfa_bwd_simple")
+    return dq, dk, dv
+
+
+def simple_device_status(stream=None) -> int:
+    """jfa_simple_device_status: status code (JFA_OK or JFA_ERR_DEVICE_TIMEOUT)."""
+    raw = ctypes.c_int()
+    return int(lib().jfa_simple_device_status(_stream(stream), ctypes.byref(raw)))
+
+
+def simple_release():
+    """Release the plans and workspaces the plan-free calls cached."""
+    _check(lib().jfa_simple_release(), "jfa_simple_release")
 
 
 def header_functions() -> list[str]:

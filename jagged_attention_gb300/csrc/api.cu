@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -631,3 +632,135 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 
+
+// ---------------------------------------------------------------------------
+// Plan-free entry points (jfa_fwd_simple / jfa_bwd_simple in jfa.h): a small
+// cache of plans keyed by device, sizes and the offsets' contents.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct SimpleEntry {
+  int device = 0, B = 0, H = 0, Lq = 0, D = 0;
+  bool broadcast = false;
+  std::vector<int32_t> kv, q;    // copies of the offsets the plan was built from
+  jfa_plan_t plan = nullptr;
+  void* ws = nullptr;            // backward workspace, allocated with the first backward
+  uint64_t last_use = 0;
+};
+
+constexpr size_t kSimpleCapacity = 8;
+std::mutex g_simple_mu;            // held for the whole of every plan-free call
+std::vector<SimpleEntry> g_simple;
+uint64_t g_simple_clock = 0;
+
+void release_entry(SimpleEntry& e) {
+  if (e.ws) cudaFree(e.ws);
+  if (e.plan) jfa_plan_destroy(e.plan);
+  e.ws = nullptr;
+  e.plan = nullptr;
+}
+
+// Checks that need no device, so bad arguments fail before any CUDA call.
+int simple_args_ok(const int32_t* kv, const int32_t* q, int B, int H, int Lq, int D) {
+  if (!kv || B < 1 || H < 1) return JFA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+  std::vector<int64_t> qlen, kvlen;
+  int64_t n_kv = 0, n_q = 0;
+  return lengths_of(kv, q, B, Lq, qlen, kvlen, &n_kv, &n_q);
+}
+
+// The cached plan for these arguments, built on a miss (the least recently
+// used entry is released when the cache is full).  Caller holds g_simple_mu.
+int simple_entry(const int32_t* kv, const int32_t* q, int B, int H, int Lq, int D, void* stream,
+                 SimpleEntry** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_CUDA;
+  const int lq = q ? 0 : Lq;
+  for (auto& e : g_simple) {
+    if (e.device == dev && e.B == B && e.H == H && e.Lq == lq && e.D == D &&
+        e.broadcast == (q == nullptr) && std::equal(e.kv.begin(), e.kv.end(), kv) &&
+        (!q || std::equal(e.q.begin(), e.q.end(), q))) {
+      e.last_use = ++g_simple_clock;
+      *out = &e;
+      return JFA_OK;
+    }
+  }
+  SimpleEntry e;
+  int rc = jfa_plan_create_ex(kv, q, B, H, Lq, D, 0, 0u, stream, &e.plan);
+  if (rc != JFA_OK) return rc;
+  e.device = dev;
+  e.B = B;
+  e.H = H;
+  e.Lq = lq;
+  e.D = D;
+  e.broadcast = q == nullptr;
+  e.kv.assign(kv, kv + B + 1);
+  if (q) e.q.assign(q, q + B + 1);
+  e.last_use = ++g_simple_clock;
+  if (g_simple.size() >= kSimpleCapacity) {
+    size_t lru = 0;
+    for (size_t i = 1; i < g_simple.size(); ++i)
+      if (g_simple[i].last_use < g_simple[lru].last_use) lru = i;
+    release_entry(g_simple[lru]);  // frees device memory: synchronises the device
+    g_simple.erase(g_simple.begin() + static_cast<std::ptrdiff_t>(lru));
+  }
+  g_simple.push_back(std::move(e));
+  *out = &g_simple.back();
+  return JFA_OK;
+}
+
+}  // namespace
+
+extern "C" int jfa_fwd_simple(const void* q, const void* k, const void* v,
+                              const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B,
+                              int H, int Lq, int D, float scale, void* out, float* lse,
+                              void* stream) {
+  int rc = simple_args_ok(kv_offsets_host, q_offsets_host, B, H, Lq, D);
+  if (rc != JFA_OK) return rc;
+  if (!std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_simple_mu);
+  SimpleEntry* e = nullptr;
+  rc = simple_entry(kv_offsets_host, q_offsets_host, B, H, Lq, D, stream, &e);
+  if (rc != JFA_OK) return rc;
+  return jfa_fwd(e->plan, q, k, v, scale, out, lse, stream);
+}
+
+extern "C" int jfa_bwd_simple(const void* q, const void* k, const void* v,
+                              const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B,
+                              int H, int Lq, int D, float scale, const void* out, const void* dout,
+                              const float* lse, float* dq, void* dk, void* dv, void* stream) {
+  int rc = simple_args_ok(kv_offsets_host, q_offsets_host, B, H, Lq, D);
+  if (rc != JFA_OK) return rc;
+  if (!std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_simple_mu);
+  SimpleEntry* e = nullptr;
+  rc = simple_entry(kv_offsets_host, q_offsets_host, B, H, Lq, D, stream, &e);
+  if (rc != JFA_OK) return rc;
+  const size_t ws_bytes = std::max<size_t>(jfa_bwd_workspace_bytes(e->plan), 256);
+  if (!e->ws && cudaMalloc(&e->ws, ws_bytes) != cudaSuccess) {
+    e->ws = nullptr;
+    return JFA_ERR_CUDA;
+  }
+  return jfa_bwd(e->plan, q, k, v, out, dout, lse, scale, dq, dk, dv, e->ws, ws_bytes, stream);
+}
+
+extern "C" int jfa_simple_device_status(void* stream, int* raw) {
+  std::lock_guard<std::mutex> lock(g_simple_mu);
+  int word = 0, rc = JFA_OK;
+  for (auto& e : g_simple) {
+    int w = 0;
+    const int r = jfa_plan_device_status(e.plan, stream, &w);
+    if (r == JFA_ERR_CUDA) return r;
+    if (r == JFA_ERR_DEVICE_TIMEOUT) rc = r;
+    word |= w;
+  }
+  if (raw) *raw = word;
+  return rc;
+}
+
+extern "C" int jfa_simple_release(void) {
+  std::lock_guard<std::mutex> lock(g_simple_mu);
+  for (auto& e : g_simple) release_entry(e);
+  g_simple.clear();
+  return JFA_OK;
+}

@@ -181,6 +181,23 @@ def test_rejects_bad_arguments_before_touching_the_device():
     assert L.jfa_bwd(None, None, None, None, None, None, None, 1.0, None, None, None, None, 0,
                      None) == 1
     assert L.jfa_status_string(7) == b"device wait timed out"
+    # plan-free entry points: argument errors come back before any CUDA call
+    kv = np.array([0, 5, 9], dtype=np.int32)
+    bad = np.array([0, 5, 3], dtype=np.int32)
+    kvp, badp = kv.ctypes.data_as(jfa._i32p), bad.ctypes.data_as(jfa._i32p)
+    fwd_args = lambda off, B, H, D, scale: (None, None, None, off, None, B, H, 4, D, scale,
+                                            None, None, None)
+    assert L.jfa_fwd_simple(*fwd_args(None, 2, 1, 128, 0.1)) == 1   # null offsets
+    assert L.jfa_fwd_simple(*fwd_args(kvp, 2, 0, 128, 0.1)) == 1    # H < 1
+    assert L.jfa_fwd_simple(*fwd_args(kvp, 2, 1, 96, 0.1)) == 2     # D not 64/128
+    assert L.jfa_fwd_simple(*fwd_args(badp, 2, 1, 128, 0.1)) == 3   # decreasing offsets
+    assert L.jfa_fwd_simple(*fwd_args(kvp, 2, 1, 128, float("nan"))) == 1
+    bwd_args = lambda off, D, scale: (None, None, None, off, None, 2, 1, 4, D, scale, None, None,
+                                      None, None, None, None, None)
+    assert L.jfa_bwd_simple(*bwd_args(badp, 128, 0.1)) == 3
+    assert L.jfa_bwd_simple(*bwd_args(kvp, 64, float("inf"))) == 1
+    assert L.jfa_simple_device_status(None, None) == 0               # nothing cached
+    assert L.jfa_simple_release() == 0
 
 
 def _rule(klen, qlen, pack):
