@@ -273,3 +273,20 @@ def test_bench_packing_matches_the_reference_packer(seed):
         want = [(b, b + n) for b, n in enumerate(pack) if n > 1]
         assert bench.packed_runs(prob, True) == want
         assert bench.packed_runs(prob, False) == []
+
+
+def test_bench_flushes_l2_only_for_small_workloads():
+    # a step whose inputs would stay in the 129 MB L2 is timed after an L2 flush
+    import types
+    import bench
+    p = workloads.make_workload("tiny_broadcast", seed=0)   # a real Problem (CPU tensors)
+    assert bench.step_input_bytes(p) == sum(t.numel() * 2 for t in (p.q, p.k, p.v, p.dout))
+    assert bench.needs_l2_flush(p)
+    for name, flush in (("jagged_self", True), ("gem_broadcast", False), ("block_diag", False),
+                        ("sparsity_0.9", False)):
+        w = workloads.WORKLOADS[name]
+        kv = workloads.offsets_from_lengths(workloads.draw_lengths(w.lengths, w.B, 0))
+        rows_q = w.Lq if w.mode == "broadcast" else int(kv[-1])
+        rows_o = w.B * w.Lq if w.mode == "broadcast" else int(kv[-1])
+        prob = types.SimpleNamespace(H=w.H, D=w.D, n_q_rows=rows_q, n_o_rows=rows_o, kv_offsets=kv)
+        assert bench.needs_l2_flush(prob) == flush, name
