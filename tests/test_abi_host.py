@@ -290,3 +290,16 @@ def test_bench_flushes_l2_only_for_small_workloads():
         rows_o = w.B * w.Lq if w.mode == "broadcast" else int(kv[-1])
         prob = types.SimpleNamespace(H=w.H, D=w.D, n_q_rows=rows_q, n_o_rows=rows_o, kv_offsets=kv)
         assert bench.needs_l2_flush(prob) == flush, name
+
+
+@pytest.mark.parametrize("lengths", [[5, 1_000_000, 300, 0, 129],      # wide cost range: comparison sort
+                                     [64] * 300 + [129, 1, 1000]])      # narrow range: counting sort
+def test_native_builder_cost_order_both_sort_paths(lengths):
+    kl = np.array(lengths, dtype=np.int64)
+    kv = workloads.offsets_from_lengths(kl)
+    for d in (0, 1):
+        for flags, dyn in ((0, False), (jfa.PLAN_DYNAMIC, True)):
+            t, p = jfa.build_tiles(kv, None, H=3, Lq=1000, num_ctas=7, direction=d, flags=flags)
+            rt, rp = ref_tiles.fwd_tiles(np.full(len(kl), 1000), kl, 3, 128, 128, 7, None, dyn) if d == 0 \
+                else ref_tiles.bwd_tiles(np.full(len(kl), 1000), kl, 3, 128, 128, 7, None, dyn)
+            assert np.array_equal(t, rt) and np.array_equal(p, rp)
