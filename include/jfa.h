@@ -3,18 +3,17 @@
  * GB300 (sm_103a).
  *
  * The operation (jagged FlashAttention pages: the alphasignal news page,
- * "GEM's sequences do not fit a fixed grid"; the PyTorch-blog summary, "JFA
- * efficiently handles jagged sequences by applying FlashAttention directly
- * to packed Q/K/V tensors and offsets"): B variable-length sequences are
- * packed back to back, with no padding, and addressed by an offsets array;
- * for every sequence b and head h
+ * section "GEM's sequences do not fit a fixed grid"; the PyTorch-blog summary
+ * on arc-codex, first key point): B variable-length sequences are packed
+ * back to back, with no padding, and addressed by an offsets array, and
+ * FlashAttention runs on them in that form; for every sequence b and head h
  *
  *     O_b = softmax(scale * Q_b K_b^T) V_b,   LSE_b = logsumexp(scale * Q_b K_b^T)
  *
  * row by row, with no mask inside a sequence.  In broadcast mode one dense
- * query block Q [Lq, H, D] attends to every sequence (same page: "GEM also
- * broadcasts one dense query across every sequence in a batch") and the
- * backward sums dQ over the batch.
+ * query block Q [Lq, H, D] attends to every sequence (same page and section:
+ * all sequences of a batch share the query block, so their query gradients
+ * add up) and the backward sums dQ over the batch.
  *
  * Layouts (all row-major, contiguous):
  *   K, V        bf16 [kv_offsets[B], H, D]
@@ -105,7 +104,7 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
 
 /*
  * JFA_PLAN_DYNAMIC: tiles are claimed at run time instead of dealt on the
- * host (the pages' dynamic balancing, which "complements" the static order):
+ * host (the pages' dynamic balancing, which works alongside the static order):
  * each schedule lists every tile once in claim order -- the tiles stably
  * sorted by their cost field, largest first -- and the plan's P CTAs take
  * tile blockIdx.x, then the next unclaimed one from a device counter, until

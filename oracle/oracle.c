@@ -5,9 +5,9 @@
  * It shares no code, header or constant with the CUDA path.
  *
  * What it computes (the jagged FlashAttention pages describe FlashAttention
- * run directly on packed Q/K/V plus an offsets tensor, with no padding: the
- * PyTorch-blog summary, "JFA efficiently handles jagged sequences ..." bullet,
- * and the asivanadi0 blog, "What it is selling").  For each sequence b and
+ * computed straight from the packed, unpadded tensors and their offsets: the
+ * PyTorch-blog summary on arc-codex, first key point, and the asivanadi0
+ * blog, section "What it is selling").  For each sequence b and
  * head h, with Q_b the query rows of b (broadcast mode: every row of the one
  * dense Q) and K_b, V_b the packed key/value rows of b:
  *

@@ -26,8 +26,9 @@ Recipes (all seeded; seed 0 is the timing seed, seeds 0-2 the parity seeds):
 The named workloads stand in for the production jagged shapes the JFA pages
 benchmark (GEM jagged / broadcast-Q shapes, the skewed-length load balancing
 case, the TLX Block Attention batch-1152, 4k-token, H=4, D=128
-block-diagonal case, the jagged broadcast-Q sparsity sweep 0.1 / 0.5 / 0.9
-and the dense B=768, H=4, D=128 case); the pages publish no dataset.
+block-diagonal case, a broadcast-Q sweep over sparsity 0.1, 0.5 and 0.9,
+and a dense case of 768 equal sequences with H=4, D=128); the pages publish
+no dataset.
 """
 from __future__ import annotations
 
