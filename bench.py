@@ -41,12 +41,11 @@ DEFAULT_WORKLOAD = "gem_broadcast"
 METRIC = "jagged attn fwd/bwd TFLOP/s (unpadded FLOPs) and % of GB300 BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch from the committed ncu captures (profiles/), keyed by
-# kernel and workload, valid only while the kernel source hash matches.
+# DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum of a
+# 256-sequence capture of the same kernel, scaled by K/V tokens: x3.730),
+# keyed by kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    # profiles/jfa_bwd_kernel_gem_broadcast_b256.md: 871.9 MB at 256 sequences, x3.730
     "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2518e+09, "src_hash": "120f0edaa62c677d"},
-    # profiles/jfa_fwd_kernel_gem_broadcast_b256.md: 478.9 MB at 256 sequences, x3.730
     "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7859e+09, "src_hash": "ac59d5daa306ef69"},
 }
 
@@ -430,7 +429,12 @@ def run_ours(args, rank, world, dist):
         return
 
     pk, pk_kind = peaks()
-    tf_peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    # The timed region lasts well under the seconds-long loop the sustained
+    # figure describes, so the kernels are held against the burst GEMM peak;
+    # a region of several seconds would take the sustained one.
+    timed_s = total_ms * 1e-3
+    sustained = timed_s >= 3.0 and "bf16_tflops_sustained" in pk
+    tf_peak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
     bw_peak = pk["hbm_gbs"]
     per_kernel = {
         "jfa_fwd_kernel": {"ms": k_fwd / args.steps, "flops": flops(prob, "fwd"),
@@ -460,7 +464,8 @@ def run_ours(args, rank, world, dist):
         roof = {"bound": "hbm", "achieved": dom["gbs"], "peak": bw_peak, "unit": "GB/s",
                 "frac": dom["gbs"] / bw_peak}
     roof.update({"traffic": traffic, "kernel": dom_name, "peak_source": f"{pk_kind} "
-                 f"({'bf16 sustained' if roof['bound'] == 'tensor' else 'hbm copy'})",
+                 f"({('bf16 sustained' if sustained else 'bf16 burst') if roof['bound'] == 'tensor' else 'hbm copy'}"
+                 f", timed region {timed_s:.2f} s)",
                  "arith_intensity": ai, "ridge": ridge,
                  "tensor_frac": dom["tensor_frac"], "hbm_frac": dom["hbm_frac"]})
 
@@ -615,6 +620,9 @@ def main():
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} needs one process per GPU (torchrun --nproc-per-node "
+                 f"{args.gpus}); this process sees WORLD_SIZE={world}")
     dist = None
     if world > 1:
         import torch.distributed as dist_
