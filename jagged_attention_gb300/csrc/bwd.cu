@@ -103,7 +103,8 @@ struct BwdBars {
   uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t dv_done, ds_empty;
   uint64_t dq_full, dq_empty;
-  uint64_t dkv_full, dkv_empty;
+  uint64_t dkv_empty;
+  uint64_t epi_done;  // a tile's last dQ has left the dS^T buffer
   uint64_t lse_ready[2], lse_done[2];  // per softmax group: LSE / Delta staging
   uint64_t dsum_part[2], dsum_ready[2];  // per softmax group: Delta formed in the kernel
   uint64_t drain;
@@ -271,10 +272,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
                     kk > 0 ? 1u : 0u);
       mma_commit(smem_u32(&bars.dq_full));  // also: Q/dO stage qs read for the last time
       mma_commit(smem_u32(&bars.ds_empty));
-      if (m == t.qblocks - 1) {
-        mma_commit(smem_u32(&bars.dkv_full));
-        mma_commit(smem_u32(&bars.kv_empty[kb]));  // K read for the last time
-      }
+      if (m == t.qblocks - 1) mma_commit(smem_u32(&bars.kv_empty[kb]));  // K read for the last time
     }
     ++tt;
   }
@@ -320,9 +318,9 @@ __device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem
   float* lse2 = reinterpret_cast<float*>(smem + C::kOffLse);  // 128 -LSE*log2(e), then 128 Delta
   float* dlt = lse2 + 128;
   const uint32_t lse_ready = smem_u32(&bars.lse_ready[g]), lse_done = smem_u32(&bars.lse_done[g]);
-  uint32_t gm = 0;
+  uint32_t gm = 0, tt = 0;
   auto next = [&] { return seq.take_warp(a.dyn_counter, bars.ring, ab); };
-  for (int i = next(); i >= 0; i = next()) {
+  for (int i = next(); i >= 0; i = next(), ++tt) {
     const BTile t = load_btile(a.tiles, i);
     // packed tile (n = -nseq): key and query rows [off[b], off[b + nseq]) of
     // nseq short sequences; a key row only meets its own sequence's queries
@@ -399,8 +397,11 @@ __device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem
       mbar_arrive(smem_u32(&bars.p_full));
 
       if (!warp_wait_b(smem_u32(&bars.dp_full), gm & 1, ab)) return;
-      // the dS^T buffer is free once the previous step's dK and dQ products completed
+      // the dS^T buffer is free once the previous step's dK and dQ products
+      // completed and, at a tile's first step, once the previous tile's last
+      // dQ has left through it
       if (!warp_wait_b(smem_u32(&bars.ds_empty), (gm & 1) ^ 1, ab)) return;
+      if (m == 0 && !warp_wait_b(smem_u32(&bars.epi_done), (tt & 1) ^ 1, ab)) return;
       tc_fence_after();
       if constexpr (kOwnDelta) {
         // The tile holds every key its queries meet, so Delta_i = sum_d dO_id
@@ -502,81 +503,15 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
 // Drain group (warps 10-13): dQ_m leaves TMEM (thread = query row), the TMEM
 // columns are released as soon as it is in shared memory, and tensor reduce-adds
 // into dq follow (the cross-batch reduction of the broadcast mode happens
-// here, in the memory system).  At the end of a tile the group writes dV and
-// scale * dK (thread = key row) before the tile's last dQ, so the next tile's
-// products do not wait for them.
-// dV and scale * dK of the tile (thread = key row), bf16.  A warp whose 32 key
-// rows all belong to the tile writes them into shared memory in the
-// 128-byte-swizzled box layout (dV in the Q stage, dK in the dO stage of the
-// step just finished, 64-column chunks 16 KB apart) and stores them as D/64
-// boxes of 32 x 64 each, dV's boxes leaving while dK is staged; a warp with
-// rows past the sequence stores its valid rows directly.  TMEM is read two
-// 32-column loads per wait.  Returns whether this warp staged (its lane 0
-// then owns open bulk groups reading the stage).
-template <int D, bool kPack>
-__device__ __forceinline__ bool dkv_epilogue(const BwdArgs& a, const CUtensorMap* dk_map,
-                                             const CUtensorMap* dv_map, uint32_t sbase, uint32_t qs,
-                                             uint32_t tl, const BTile& t, int wq, int lane,
-                                             uint32_t dkv_empty) {
-  using C = BwdCfg<D>;
-  const int H = a.pb.H;
-  const int r = wq * 32 + lane;
-  const bool packed = kPack && t.n < 0;  // packed tile: rows of -n short sequences
+// here, in the memory system).  At the end of a tile the group also writes dV
+// and scale * dK (thread = key row) as bf16 boxes of 32 x 64.
+// Whether key row r of tile t belongs to the tile's sequence(s).
+template <bool kPack>
+__device__ __forceinline__ bool key_row_ok(const BwdArgs& a, const BTile& t, int r) {
+  const bool packed = kPack && t.n < 0;
   const int nb = packed ? 0 : t.n;
   const int64_t klen = a.pb.kv_off[t.b + (packed ? -t.n : 1)] - a.pb.kv_off[t.b];
-  const bool kv_ok = int64_t(nb) * 128 + r < klen;
-  const bool whole = __all_sync(0xffffffffu, kv_ok);
-  const int64_t krow = int64_t(a.pb.kv_off[t.b]) + nb * 128 + r;
-  const int y = static_cast<int>(int64_t(a.pb.kv_off[t.b]) + nb * 128 + wq * 32);  // first row of the boxes
-#pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
-    const float mul = which == 0 ? 1.0f : a.scale;
-    uint16_t* dst_row = (which == 0 ? a.dv : a.dk) + (krow * H + t.h) * D;
-    const uint32_t region = sbase + (which == 0 ? C::kOffQ : C::kOffDO) + qs * C::kTileBytes + wq * 4096;
-#pragma unroll
-    for (int c2 = 0; c2 < D / 32; c2 += 2) {
-      uint32_t ww[2][32];
-      tmem_ld_x32_nw(tl + col + c2 * 32, ww[0]);
-      tmem_ld_x32_nw(tl + col + (c2 + 1) * 32, ww[1]);
-      tmem_ld_wait2(ww[0], ww[1]);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = c2 + h;
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(ww[h][2 * e]) * mul, __uint_as_float(ww[h][2 * e + 1]) * mul);
-        if (whole) {
-          // 32 columns = units 4(c&1) .. 4(c&1)+3 of the row in chunk c/2
-          const uint32_t dst = region + lane * 128 + (c >> 1) * 16384;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st_shared_v4(dst + (((4 * (c & 1) + q) ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
-                         pk[4 * q + 2], pk[4 * q + 3]);
-        } else if (kv_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        }
-      }
-    }
-    if (which == 1) {
-      tc_fence_before();
-      mbar_arrive(dkv_empty);  // dK / dV TMEM columns free for the next tile
-    }
-    if (whole) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_store_2d(which == 0 ? dv_map : dk_map, region + c * 16384, t.h * D + c * 64, y);
-        bulk_commit();
-      }
-    }
-  }
-  return whole;
+  return int64_t(nb) * 128 + r < klen;
 }
 
 // 32 dQ columns of one row: reduce-added, or stored when this tile owns the row.
@@ -625,18 +560,9 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
     const int64_t q_base = a.pb.q_off ? a.pb.q_off[t.b] : 0;
     for (int m = 0; m < t.qblocks; ++m, ++gm) {
       const uint32_t qs = gm & 1;
-      if (m == t.qblocks - 1) {
-        // dkv_full fires with this step's dq_full: the Q/dO stage is free
-        if (!warp_wait_b(smem_u32(&bars.dkv_full), tt & 1, ab)) return;
-        tc_fence_after();
-        const bool staged = dkv_epilogue<D, kPack>(a, dk_map, dv_map, sbase, qs, tl, t, wq, lane,
-                                                   smem_u32(&bars.dkv_empty));
-        if (staged && lane == 0) bulk_wait_read_all();  // the stage is reused for dQ below
-        __syncwarp();
-        ++tt;
-      }
       if (!warp_wait_b(smem_u32(&bars.dq_full), gm & 1, ab)) return;
       tc_fence_after();
+      const bool last = m == t.qblocks - 1;
       const bool q_ok = int64_t(m) * 128 + r < qlen;
       const bool whole = __all_sync(0xffffffffu, q_ok);
       float* row = a.dq + ((q_base + int64_t(m) * 128 + r) * H + t.h) * D;
@@ -645,46 +571,156 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
                                    : C::kOffDO + qs * C::kTileBytes + (k - D / 64) * 16384) +
                wq * 4096;
       };
-#pragma unroll
-      for (int k2 = 0; k2 < D / 32; k2 += 2) {
-        uint32_t vv[2][32];
+      uint32_t vv[2][32];
+      auto load_pair = [&](int k2) {
         tmem_ld_x32_nw(tl + C::kColDP + k2 * 32, vv[0]);
         tmem_ld_x32_nw(tl + C::kColDP + (k2 + 1) * 32, vv[1]);
         tmem_ld_wait2(vv[0], vv[1]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int k = k2 + h;
-          const uint32_t (&v)[32] = vv[h];
-          if (whole) {
-            const uint32_t dst = box_addr(k) + lane * 128;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              st_shared_v4(dst + ((u ^ (lane & 7)) << 4),
-                           __float_as_uint(__uint_as_float(v[4 * u]) * a.scale),
-                           __float_as_uint(__uint_as_float(v[4 * u + 1]) * a.scale),
-                           __float_as_uint(__uint_as_float(v[4 * u + 2]) * a.scale),
-                           __float_as_uint(__uint_as_float(v[4 * u + 3]) * a.scale));
-          } else if (q_ok) {
-            dq_row_out(row + k * 32, v, a.scale, store);
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.dq_empty));  // dQ TMEM columns free for the next dP
-      if (whole) fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
+      };
+      auto put = [&](int k, uint32_t dst_box, const uint32_t (&v)[32]) {  // dQ columns [32k, 32k + 32)
         if (whole) {
-          const int y = static_cast<int>(q_base + int64_t(m) * 128 + wq * 32);
+          const uint32_t dst = dst_box + lane * 128;
 #pragma unroll
-          for (int k = 0; k < D / 32; ++k) {
-            if (store) tma_store_2d(dq_map, box_addr(k), t.h * D + k * 32, y);
-            else tma_reduce_add_2d(dq_map, box_addr(k), t.h * D + k * 32, y);
-          }
-          bulk_commit();
-          bulk_wait_read_all();
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(dst + ((u ^ (lane & 7)) << 4),
+                         __float_as_uint(__uint_as_float(v[4 * u]) * a.scale),
+                         __float_as_uint(__uint_as_float(v[4 * u + 1]) * a.scale),
+                         __float_as_uint(__uint_as_float(v[4 * u + 2]) * a.scale),
+                         __float_as_uint(__uint_as_float(v[4 * u + 3]) * a.scale));
+        } else if (q_ok) {
+          dq_row_out(row + k * 32, v, a.scale, store);
         }
-        mbar_arrive(smem_u32(&bars.q_empty[qs]));
+      };
+      const int y = static_cast<int>(q_base + int64_t(m) * 128 + wq * 32);
+      auto send = [&](int k, uint32_t src_box) {  // lane 0: one box out
+        if (store) tma_store_2d(dq_map, src_box, t.h * D + k * 32, y);
+        else tma_reduce_add_2d(dq_map, src_box, t.h * D + k * 32, y);
+      };
+      if (!last) {
+#pragma unroll
+        for (int k2 = 0; k2 < D / 32; k2 += 2) {
+          load_pair(k2);
+          put(k2, box_addr(k2), vv[0]);
+          put(k2 + 1, box_addr(k2 + 1), vv[1]);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_empty));  // dQ TMEM columns free for the next dP
+        if (whole) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (whole) {
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) send(k, box_addr(k));
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(smem_u32(&bars.q_empty[qs]));
+        }
+      } else {
+        // A tile's last step (dq_full: dV and dK are complete too): dQ, dV and
+        // dK leave together, and the next tile's first dP and first dV wait
+        // for their TMEM columns, while boxes take a while to be read out of
+        // shared memory (the memory system drains reduce-adds slowly).  So
+        // every TMEM read comes first: dQ's first half goes out through the
+        // dO half of the stage, its second through the dS^T buffer (the
+        // next tile's first dS^T waits for epi_done), dV through the Q half,
+        // and dK waits in registers as bf16 until dQ's first half is read out.
+        const uint32_t do_box = sbase + C::kOffDO + qs * C::kTileBytes + wq * 4096;  // box j at + j * 16384
+        const uint32_t ds_box = sbase + C::kOffDS + wq * 4096;
+        constexpr int kHalf = D / 64;  // dQ boxes per half
+#pragma unroll
+        for (int k2 = 0; k2 < D / 32; k2 += 2) {
+          load_pair(k2);
+          const uint32_t base = k2 < kHalf ? do_box + k2 * 16384 : ds_box + (k2 - kHalf) * 16384;
+          put(k2, base, vv[0]);
+          put(k2 + 1, kHalf == 1 ? ds_box : base + 16384, vv[1]);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dq_empty));
+        if (whole) fence_proxy_async_smem();
+        __syncwarp();
+        if (whole && lane == 0) {  // group 1: the dO-half boxes, group 2: the dS^T-buffer boxes
+#pragma unroll
+          for (int j = 0; j < kHalf; ++j) send(j, do_box + j * 16384);
+          bulk_commit();
+#pragma unroll
+          for (int j = 0; j < kHalf; ++j) send(kHalf + j, ds_box + j * 16384);
+          bulk_commit();
+        }
+        // dV through the Q half (group 3), dK into registers
+        const bool kv_ok = key_row_ok<kPack>(a, t, r);
+        const bool kv_whole = __all_sync(0xffffffffu, kv_ok);
+        const int nb = (kPack && t.n < 0) ? 0 : t.n;
+        const int64_t krow = int64_t(a.pb.kv_off[t.b]) + nb * 128 + r;
+        const int yk = static_cast<int>(int64_t(a.pb.kv_off[t.b]) + nb * 128 + wq * 32);
+        const uint32_t qh = sbase + C::kOffQ + qs * C::kTileBytes + wq * 4096;  // chunk c at + c * 16384
+        auto put_bf16 = [&](uint32_t region, uint16_t* dst_row, int c, const uint32_t (&pk)[16]) {
+          if (kv_whole) {  // 32 columns = units 4(c&1) .. 4(c&1)+3 of the row in chunk c/2
+            const uint32_t dst = region + lane * 128 + (c >> 1) * 16384;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(dst + (((4 * (c & 1) + q) ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                           pk[4 * q + 2], pk[4 * q + 3]);
+          } else if (kv_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        };
+        uint16_t* dv_row = a.dv + (krow * H + t.h) * D;
+        uint16_t* dk_row = a.dk + (krow * H + t.h) * D;
+#pragma unroll
+        for (int c2 = 0; c2 < D / 32; c2 += 2) {
+          uint32_t ww[2][32];
+          tmem_ld_x32_nw(tl + C::kColDV + c2 * 32, ww[0]);
+          tmem_ld_x32_nw(tl + C::kColDV + (c2 + 1) * 32, ww[1]);
+          tmem_ld_wait2(ww[0], ww[1]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(__uint_as_float(ww[h][2 * e]), __uint_as_float(ww[h][2 * e + 1]));
+            put_bf16(qh, dv_row, c2 + h, pk);
+          }
+        }
+        uint32_t dkp[D / 32][16];  // scale * dK of this row, bf16 pairs
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t w[32];
+          tmem_ld_x32(tl + C::kColDK + c * 32, w);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            dkp[c][e] = pack_bf16x2(__uint_as_float(w[2 * e]) * a.scale, __uint_as_float(w[2 * e + 1]) * a.scale);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.dkv_empty));  // dV / dK columns free for the next tile
+        if (kv_whole) fence_proxy_async_smem();
+        __syncwarp();
+        if (kv_whole && lane == 0) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) tma_store_2d(dv_map, qh + c * 16384, t.h * D + c * 64, yk);
+          bulk_commit();
+          if (whole) bulk_wait_read_keep2();  // dQ's dO-half boxes are read out
+        }
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) put_bf16(do_box, dk_row, c, dkp[c]);
+        if (kv_whole) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (kv_whole) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_store_2d(dk_map, do_box + c * 16384, t.h * D + c * 64, yk);
+            bulk_commit();
+          }
+          // open groups, oldest first: dQ dO half, dQ dS^T buffer, dV, dK
+          if (whole && kv_whole) bulk_wait_read_keep2();
+          else if (whole) bulk_wait_read_all();
+          mbar_arrive(smem_u32(&bars.epi_done));  // the dS^T buffer is read out
+          bulk_wait_read_all();                   // the stage is read out
+          mbar_arrive(smem_u32(&bars.q_empty[qs]));
+        }
+        ++tt;
       }
       __syncwarp();
     }
@@ -722,8 +758,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(smem_u32(&bars.ds_empty), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
     mbar_init(smem_u32(&bars.dq_empty), 128);
-    mbar_init(smem_u32(&bars.dkv_full), 1);
     mbar_init(smem_u32(&bars.dkv_empty), 128);
+    mbar_init(smem_u32(&bars.epi_done), 4);  // one arrival per drain warp
     for (int g = 0; g < 2; ++g) {
       mbar_init(smem_u32(&bars.lse_ready[g]), 128);
       mbar_init(smem_u32(&bars.lse_done[g]), 128);
