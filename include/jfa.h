@@ -246,8 +246,12 @@ int jfa_plan_device_status(jfa_plan_t plan, void* stream, int* raw);
  * of Delta plus 16 bytes per backward tile; no Delta where the tiles form it,
  * under the default rule given with JFA_PLAN_DELTA_PREPASS) does not fit is
  * rejected with
- * JFA_ERR_WORKSPACE before anything is launched.  The call allocates no
- * device memory and calls no allocating library routine.
+ * JFA_ERR_WORKSPACE before anything is launched, as is (JFA_ERR_UNSUPPORTED)
+ * any problem jfa_plan_create would refuse.  The call allocates no device
+ * memory and calls no allocating library routine.  It uploads the schedule
+ * and offsets with cudaMemcpyAsync from a host buffer that lives only for
+ * the call (pageable memory), so the call returns once that copy has been
+ * taken from the host buffer.
  *
  * The first call on a device resolves the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
@@ -261,6 +265,25 @@ int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
                     int Lq, int D, const void* q, const void* k, const void* v, const void* out,
                     const void* dout, const float* lse, float scale, float* dq, void* dk, void* dv,
                     int* device_status, void* stream);
+
+/*
+ * Test of the kernels' failure path (no counterpart in the pages; it exists
+ * so that the timeout handling of the real kernels can be exercised on a GPU
+ * without a fault).  Sets, for the plan's later launches, a limit of
+ * limit_us microseconds on every device wait (0: the normal 2 s; at most
+ * 2,000,000) and, with skip != 0, has one softmax warp of CTA 0 withhold one
+ * arrival so that a wait of the MMA issuer runs out:
+ *   skip = 1  jfa_fwd: the arrival on the first P block of CTA 0's first tile
+ *   skip = 2  jfa_bwd: the arrival on the first dS^T block of CTA 0
+ *   skip = 0  nothing withheld (normal operation)
+ * The wait that runs out raises the CTA's abort flag: every role leaves its
+ * loop, the TMA producer and the MMA issuer wait (bounded) for their work in
+ * flight, and the TMEM is freed before the CTA exits, so the context stays
+ * usable; jfa_plan_device_status then reports JFA_ERR_DEVICE_TIMEOUT, and the
+ * outputs of that launch are undefined.  Not for production use: nothing in
+ * the library or its benchmark sets it.  Errors: JFA_ERR_INVALID_ARG.
+ */
+int jfa_plan_selftest(jfa_plan_t plan, int skip, unsigned limit_us);
 
 /*
  * Self-test of the failure path (no counterpart in the pages; it exists so

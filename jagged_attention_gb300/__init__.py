@@ -88,12 +88,14 @@ def lib() -> ctypes.CDLL:
             L.jfa_simple_device_status.argtypes = [_vp, _ip]
             L.jfa_simple_release.argtypes = []
             L.jfa_plan_device_status.argtypes = [_vp, _vp, _ip]
+            L.jfa_plan_selftest.argtypes = [_vp, ctypes.c_int, ctypes.c_uint]
             L.jfa_status_string.argtypes = [ctypes.c_int]
             L.jfa_status_string.restype = ctypes.c_char_p
             for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
                          "jfa_fwd", "jfa_bwd", "jfa_bwd_preprocess", "jfa_bwd_main",
                          "jfa_plan_device_status", "jfa_delta_in_tiles", "jfa_fwd_simple",
-                         "jfa_bwd_simple", "jfa_simple_device_status", "jfa_simple_release"):
+                         "jfa_bwd_simple", "jfa_simple_device_status", "jfa_simple_release",
+                         "jfa_plan_selftest"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -215,6 +217,12 @@ class Plan:
         _check(lib().jfa_plan_device_status(self.handle, _stream(stream), ctypes.byref(raw)),
                "jfa_plan_device_status")
         return raw.value
+
+    def selftest(self, skip: int, limit_us: int = 0):
+        """Failure-path test only (jfa_plan_selftest): shorten every device wait of
+        this plan's later launches to limit_us and withhold one arrival (skip 1:
+        forward, 2: backward; 0: none)."""
+        _check(lib().jfa_plan_selftest(self.handle, skip, limit_us), "jfa_plan_selftest")
 
     def close(self):
         if self._h is not None:

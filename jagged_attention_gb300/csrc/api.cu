@@ -337,6 +337,13 @@ int jfa_plan_destroy(jfa_plan_t plan) {
   return rc;
 }
 
+int jfa_plan_selftest(jfa_plan_t plan, int skip, unsigned limit_us) {
+  if (!plan || skip < 0 || skip > 2 || limit_us > 2000000u) return JFA_ERR_INVALID_ARG;
+  plan->test_skip = skip;
+  plan->test_limit_ns = uint64_t(limit_us) * 1000u;
+  return JFA_OK;
+}
+
 int jfa_plan_tiles(jfa_plan_t plan, int dir, int32_t* tiles_host, int32_t* cta_ptr_host, int* T,
                    int* P) {
   if (!plan || (dir != 0 && dir != 1) || !T || !P) return JFA_ERR_INVALID_ARG;
@@ -386,6 +393,8 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
   a.status = plan->d_status;
   a.packed = plan->packed;
   a.T = plan->fwd.T;
+  a.wait_limit_ns = plan->test_limit_ns;
+  a.test_skip = plan->test_skip == 1 ? 1 : 0;
   if (plan->dynamic) {
     a.dyn_counter = plan->d_counters;
     if (cudaMemsetAsync(a.dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -472,6 +481,8 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
   a.own_rows = plan->dq_own_rows;
   a.own_delta = plan->own_delta;
   a.T = plan->bwd.T;
+  a.wait_limit_ns = plan->test_limit_ns;
+  a.test_skip = plan->test_skip == 2 ? 2 : 0;
   if (plan->dynamic) {
     a.dyn_counter = plan->d_counters + 1;
     if (cudaMemsetAsync(a.dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -536,7 +547,8 @@ extern "C" int jfa_bwd_noalloc(const int32_t* kv_offsets_host, const int32_t* q_
   int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
   if (rc != JFA_OK) return rc;
   const int64_t n_o = q_offsets_host ? n_q : int64_t(B) * Lq;
-  if (n_o >= (int64_t(1) << 31)) return JFA_ERR_UNSUPPORTED;
+  if (n_o >= (int64_t(1) << 31) || int64_t(H) * D * 2 >= (int64_t(1) << 31))
+    return JFA_ERR_UNSUPPORTED;
   if ((n_q > 0 && (!q || !dq)) || (n_kv > 0 && (!k || !v || !dk || !dv)) ||
       (n_o > 0 && (!out || !dout || !lse)))
     return JFA_ERR_INVALID_ARG;

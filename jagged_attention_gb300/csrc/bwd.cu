@@ -484,7 +484,9 @@ __device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.ds_full));
+      // (failure-path test: CTA 0's first warp withholds its first arrival)
+      if (!(a.test_skip == 2 && blockIdx.x == 0 && warp == 0 && gm == 0))
+        mbar_arrive(smem_u32(&bars.ds_full));
       mbar_arrive(lse_done);  // this block's LSE / Delta no longer read by this thread
     }
   }
@@ -778,7 +780,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
-  const Abort ab{&bars.abort_flag, a.status};
+  const Abort ab{&bars.abort_flag, a.status, a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs};
   TileSeq<kDyn> seq(a.cta_ptr, a.dyn_counter);
   if (warp < 8) {
     bwd_softmax<D, kPack>(a, smem, sbase, tmem, bars, ab, seq, warp >> 2);

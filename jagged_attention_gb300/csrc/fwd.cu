@@ -382,7 +382,9 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
       tmem_st_x32(tl + C::kColP + sb * 64 + grp * 32, p);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.p_full[sb]));
+      // (failure-path test: CTA 0's first warp withholds its first arrival)
+      if (!(a.test_skip == 1 && blockIdx.x == 0 && warp == 0 && gj == 0))
+        mbar_arrive(smem_u32(&bars.p_full[sb]));
       m_run = m_new;
     }
     // epilogue: combine the groups' row sums, wait for the last PV,
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
-  const Abort ab{&bars.abort_flag, a.status};
+  const Abort ab{&bars.abort_flag, a.status, a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs};
   TileSeq<kDyn> seq(a.cta_ptr, a.dyn_counter);
 
   if (warp == C::kProducerWarp) {

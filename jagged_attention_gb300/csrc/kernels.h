@@ -27,6 +27,10 @@ struct FwdArgs {
   bool packed;             // the schedule may hold packed tiles {b0, h, -nseq, 1}
   int* dyn_counter = nullptr;  // dynamic schedule: claim counter (zeroed before the launch)
   int T = 0;                   // tiles in the schedule
+  // failure-path test only (jfa_plan_selftest): a limit for every wait
+  // (0: the default) and, with test_skip = 1, one arrival withheld
+  uint64_t wait_limit_ns = 0;
+  int test_skip = 0;
 };
 
 struct BwdArgs {
@@ -48,6 +52,8 @@ struct BwdArgs {
                            // kernel forms Delta itself and `delta` is not read
   int* dyn_counter = nullptr;  // dynamic schedule: claim counter (zeroed before the launch)
   int T = 0;                   // tiles in the schedule
+  uint64_t wait_limit_ns = 0;  // failure-path test only, as in FwdArgs (test_skip = 2)
+  int test_skip = 0;
 };
 
 // Forward: one persistent launch over the schedule (grid = P CTAs).  o_map:

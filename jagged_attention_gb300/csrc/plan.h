@@ -62,6 +62,9 @@ struct jfa_plan {
   // tile meets all the keys of its queries and forms Delta itself: the
   // pre-pass skips the Delta kernel (unless JFA_PLAN_DELTA_PREPASS)
   bool own_delta = false;
+  // failure-path test only (jfa_plan_selftest)
+  int test_skip = 0;
+  uint64_t test_limit_ns = 0;
   int* d_counters = nullptr; // dynamic: claim counters [fwd, bwd]
   int device = 0;
   int num_ctas = 0;

@@ -65,13 +65,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 struct Abort {
   volatile int* flag;   // shared memory
   int* status;          // global memory
+  uint64_t limit_ns = kWaitLimitNs;  // how long one wait may last
 };
 
 // Wait until the phase with the given parity has completed.  Returns false
 // (and raises the CTA's abort flag and the device status) when the wait runs
 // past kWaitLimitNs, or when another role of the CTA has already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab,
-                                          uint64_t limit_ns = kWaitLimitNs) {
+                                          uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -85,6 +86,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  return mbar_wait(bar, parity, ab, ab.limit_ns);
 }
 
 // ---------------------------------------------------------------------------

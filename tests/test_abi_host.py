@@ -221,6 +221,24 @@ def _rule(klen, qlen, pack):
     return tiles > 0 and rows >= 96 * tiles
 
 
+def test_noalloc_refuses_what_a_plan_refuses_before_touching_the_device():
+    """jfa_bwd_noalloc checks its sizes as jfa_plan_create does, before any CUDA
+    call: H * D * 2 bytes per row must stay below 2^31, and D must be 64 or 128."""
+    import ctypes
+    L = jfa.lib()
+    fn = L.jfa_bwd_noalloc
+    fn.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    fn.argtypes = [jfa._i32p, jfa._i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp]
+    kv = jfa._offsets([0, 3])
+    args = lambda H, D: (jfa._i32ptr(kv), None, 1, H, 2, D, None, None, None, None, None, None,
+                         0.125, None, None, None, None, None)
+    assert fn(*args(1 << 24, 64)) == 2   # 2^24 heads x 64 x 2 bytes = 2^31: JFA_ERR_UNSUPPORTED
+    assert fn(*args(1, 96)) == 2         # D not in {64, 128}
+    assert fn(*args(0, 64)) == 1         # no heads: JFA_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_delta_path_follows_the_documented_rule(seed):
     rng = np.random.default_rng(seed)

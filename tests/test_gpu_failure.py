@@ -35,3 +35,42 @@ def test_wait_timeout_is_reported_and_context_survives(limit_us):
     O_ref, L_ref = parity.oracle_fwd(p)
     parity.check_fwd(out, lse, O_ref, L_ref)
     assert plan.device_status() == 0
+
+
+def test_plan_selftest_rejects_bad_arguments():
+    # host-side checks only (no plan, bad codes and limits): runs without a GPU
+    L = jfa.lib()
+    assert L.jfa_plan_selftest(None, 1, 1000) == JFA_ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("skip", [1, 2])
+def test_real_kernel_timeout_cascade(skip):
+    """One softmax warp of CTA 0 withholds one arrival (skip 1: the forward's
+    first P block, 2: the backward's first dS^T), with every wait limited to
+    20 ms: the MMA issuer's wait runs out, the abort reaches every role of the
+    CTA (producer drain, MMA drain commit, TMEM release), the launch ends, the
+    plan's status word reports JFA_ERR_DEVICE_TIMEOUT, and a normal forward
+    and backward right after still match the oracle."""
+    import torch
+    p = parity.to_cuda(workloads.make_workload("tiny_broadcast", seed=0))
+    plan = parity.make_plan(p)
+    out, lse, _ = parity.gpu_fwd(p, plan)
+    plan.selftest(skip, 20000)
+    if skip == 1:
+        o2 = torch.empty_like(out)
+        l2 = torch.empty_like(lse)
+        jfa.fwd(plan, p.q, p.k, p.v, p.scale, out=o2, lse=l2)
+    else:
+        dq = torch.empty(p.q.shape, dtype=torch.float32, device="cuda")
+        dk, dv = torch.empty_like(p.k), torch.empty_like(p.v)
+        jfa.bwd(plan, p.q, p.k, p.v, out, p.dout, lse, p.scale, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    with pytest.raises(jfa.JfaError) as err:
+        plan.device_status()
+    assert err.value.code == JFA_ERR_DEVICE_TIMEOUT
+    plan.selftest(0, 0)
+    out, lse, _ = parity.gpu_fwd(p, plan)  # asserts a clean status word
+    parity.check_fwd(out, lse, *parity.oracle_fwd(p))
+    dq, dk, dv = parity.gpu_bwd(p, out, lse, plan)
+    parity.check_grads(dq, dk, dv, *parity.oracle_bwd(p))

@@ -1,89 +1,162 @@
-"""Full-size parity: the GEM-like broadcast, skewed broadcast and
-block-diagonal workloads at their full sizes, run in the launch configuration
-bench.py times (one persistent CTA per SM), checked against the fp64 oracle
-on sampled outputs it computes one by one:
+"""Full-size parity, element by element: the GEM-like broadcast, skewed
+broadcast and block-diagonal workloads at their full sizes, run in the launch
+configuration bench.py times (one persistent CTA per SM), against the fp64
+oracle on every output element.
 
-* every output row written and finite (outputs are NaN-prefilled);
-* O and LSE of sampled (sequence, head) pairs: the shortest, the longest and
-  random sequences;
-* dK and dV of the same pairs (the oracle's per-sequence backward);
-* dQ: broadcast mode sums over every sequence, so sampled query rows are
-  recomputed row by row over the whole batch of one head; self mode takes the
-  sampled sequences' rows.
+The oracle runs over the batch in chunks of whole sequences (a few hundred
+thousand key rows at a time, so its fp64 copies stay a few GB); each chunk's
+O, LSE, dK and dV are compared with the GPU's rows of the same sequences, and
+in broadcast mode the chunks' dQ are summed into the one batch-wide dQ the
+GPU reduces.  Each workload runs its plan variants (schedule flags) on the
+GPU first, and the oracle pass checks all of them.
+
+Bounds (bf16 inputs and outputs, fp32 accumulation):
+* O: max-abs error <= 1e-2 over every element; LSE: max-abs <= 1e-3;
+* dQ, dK, dV: relative L2 <= 1e-2 over the whole tensor;
+* and, so that an error confined to a few tiles cannot hide in the whole
+  tensor's norm, relative L2 <= 2e-2 for every (sequence, head) block of dK,
+  dV (and of dQ in self mode), its denominator floored at 1e-3 of the
+  blocks' RMS norm so that blocks whose exact gradient vanishes (a one-key
+  sequence has dK = 0) are held to an absolute bound instead.
+Every output is NaN-prefilled and guard-banded (tests/parity.py).
 """
 import numpy as np
 import pytest
 import torch
 
+import jagged_attention_gb300 as jfa
 import oracle
 import workloads
 from tests import parity
 
 pytestmark = pytest.mark.gpu
 
+VARIANTS = {
+    "gem_broadcast": [0, jfa.PLAN_DYNAMIC],
+    "skewed_broadcast": [0],
+    "block_diag": [0, jfa.PLAN_PACK_SHORT, jfa.PLAN_PACK_SHORT | jfa.PLAN_DYNAMIC],
+}
+CHUNK_KV_ROWS = 1 << 17
+LOCAL_TOL = 2e-2
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
-    import jagged_attention_gb300 as jfa
     jfa.build()
 
 
-def _sampled_sequences(p, rng, n_random=3):
-    klen = p.kv_lengths
-    nonempty = np.nonzero(klen > 0)[0]
-    picks = {int(nonempty[np.argmin(klen[nonempty])]), int(np.argmax(klen))}
-    picks.update(int(b) for b in rng.choice(nonempty, size=min(n_random, nonempty.size), replace=False))
-    return sorted(picks)
+def _chunks(kvo: np.ndarray, max_rows: int):
+    """Sequence ranges [b, e) holding at most max_rows key rows (at least one sequence)."""
+    B = kvo.size - 1
+    b = 0
+    while b < B:
+        e = b + 1
+        while e < B and kvo[e + 1] - kvo[b] <= max_rows:
+            e += 1
+        yield b, e
+        b = e
 
 
-@pytest.mark.parametrize("name,flags", [("gem_broadcast", 0), ("skewed_broadcast", 0),
-                                        ("block_diag", 0), ("block_diag", 1),
-                                        ("gem_broadcast", 2), ("block_diag", 3)])
-def test_full_size_sampled_parity(name, flags):
+def _blocks(got: np.ndarray, ref: np.ndarray, offsets: np.ndarray):
+    """Squared error and squared reference norm per (non-empty sequence, head)."""
+    err2 = ((got - ref) ** 2).sum(axis=2)
+    ref2 = (ref ** 2).sum(axis=2)
+    starts = offsets[:-1][np.diff(offsets) > 0]
+    if starts.size == 0:
+        return np.zeros((0, got.shape[1])), np.zeros((0, got.shape[1]))
+    return np.add.reduceat(err2, starts, axis=0), np.add.reduceat(ref2, starts, axis=0)
+
+
+class _Tally:
+    """Running whole-tensor and per-block error statistics of one gradient."""
+
+    def __init__(self):
+        self.err2 = 0.0
+        self.ref2 = 0.0
+        self.blocks_e, self.blocks_r = [], []
+
+    def add(self, got, ref, offsets):
+        g = got.astype(np.float64)
+        self.err2 += float(((g - ref) ** 2).sum())
+        self.ref2 += float((ref ** 2).sum())
+        e, r = _blocks(g, ref, offsets)
+        self.blocks_e.append(e)
+        self.blocks_r.append(r)
+
+    def check(self, name):
+        rel = np.sqrt(self.err2 / self.ref2) if self.ref2 > 0 else np.sqrt(self.err2)
+        assert rel <= parity.TOL_GRAD, f"{name}: whole-tensor relative L2 {rel:.3e}"
+        e = np.concatenate(self.blocks_e)
+        r = np.concatenate(self.blocks_r)
+        if e.size:
+            floor = 1e-3 * np.sqrt(r.mean())
+            local = np.sqrt(e) / np.maximum(np.sqrt(r), floor)
+            worst = np.unravel_index(np.argmax(local), local.shape)
+            assert local.max() <= LOCAL_TOL, (
+                f"{name}: (sequence, head) block {worst} relative L2 {local.max():.3e}")
+        return rel
+
+
+@pytest.mark.parametrize("name", sorted(VARIANTS))
+def test_full_size_every_element(name):
     torch.cuda.empty_cache()
     orc = oracle.default()
-    rng = np.random.default_rng(123)
     p = workloads.make_workload(name, seed=0, device="cuda")
-    plan = parity.make_plan(p, flags=flags)  # num_ctas = SM count, as bench.py runs it
-    out, lse, _ = parity.gpu_fwd(p, plan)
-    dq, dk, dv = parity.gpu_bwd(p, out, lse, plan)
-
-    assert torch.isfinite(out.float()).all(), "O has unwritten rows"
-    assert not torch.isnan(lse).any(), "LSE has unwritten rows"
-    for t, n in ((dq, "dQ"), (dk, "dK"), (dv, "dV")):
-        assert torch.isfinite(t.float()).all(), f"{n} has unwritten or non-finite entries"
+    runs = {}
+    for flags in VARIANTS[name]:
+        plan = parity.make_plan(p, flags=flags)  # num_ctas = SM count, as bench.py runs it
+        out, lse, _ = parity.gpu_fwd(p, plan)
+        dq, dk, dv = parity.gpu_bwd(p, out, lse, plan)
+        runs[flags] = (out, lse, dq, dk, dv)
+        plan.close()
 
     kvo = p.kv_offsets.astype(np.int64)
-    for b in _sampled_sequences(p, rng):
-        h = int(rng.integers(p.H))
-        ks, ke = int(kvo[b]), int(kvo[b + 1])
+    qo = None if p.q_offsets is None else p.q_offsets.astype(np.int64)
+    H, D, Lq = p.H, p.D, p.Lq
+    o_err = {f: 0.0 for f in runs}
+    l_err = {f: 0.0 for f in runs}
+    tallies = {f: {g: _Tally() for g in ("dK", "dV", "dQ")} for f in runs}
+    dq_sum = np.zeros((Lq, H, D)) if p.mode == "broadcast" else None
+    for b, e in _chunks(kvo, CHUNK_KV_ROWS):
+        ks, ke = int(kvo[b]), int(kvo[e])
+        kv_sub = kvo[b:e + 1] - kvo[b]
+        k, v = p.k[ks:ke].cpu(), p.v[ks:ke].cpu()
         if p.mode == "broadcast":
-            qs, qe = 0, p.Lq
-            os_, oe = b * p.Lq, (b + 1) * p.Lq
+            q, q_sub, qs, qe = p.q.cpu(), None, 0, Lq
+            os_, oe = b * Lq, e * Lq
         else:
-            qs, qe = int(p.q_offsets[b]), int(p.q_offsets[b + 1])
+            qs, qe = int(qo[b]), int(qo[e])
+            q_sub = qo[b:e + 1] - qo[b]
+            q = p.q[qs:qe].cpu()
             os_, oe = qs, qe
-        q = p.q[qs:qe, h].cpu()
-        k = p.k[ks:ke, h].cpu()
-        v = p.v[ks:ke, h].cpu()
-        g = p.dout[os_:oe, h].cpu()
-        O_ref, L_ref = orc.seq_fwd(q, k, v, p.scale)
-        assert (out[os_:oe, h].cpu().double() - O_ref).abs().max().item() <= parity.TOL_O
-        assert (lse[h, os_:oe].cpu().double() - L_ref).abs().max().item() <= parity.TOL_LSE
-        dq_b, dk_ref, dv_ref = orc.seq_bwd(q, k, v, g, p.scale)
-        assert parity.rel_l2(dk[ks:ke, h], dk_ref) <= parity.TOL_GRAD, ("dK", b, h)
-        assert parity.rel_l2(dv[ks:ke, h], dv_ref) <= parity.TOL_GRAD, ("dV", b, h)
-        if p.mode == "self":
-            assert parity.rel_l2(dq[qs:qe, h], dq_b) <= parity.TOL_GRAD, ("dQ", b, h)
-
-    if p.mode == "broadcast":
-        # dQ rows summed over the whole batch for one head, recomputed row by row
-        h = int(rng.integers(p.H))
-        rows = np.array([0, 127, 128, p.Lq - 1] + list(rng.integers(0, p.Lq, size=2)))
-        one = lambda t: t[:, h:h + 1].contiguous().cpu()
-        ref = orc.dq_rows(one(p.q), one(p.k), one(p.v), one(p.dout), p.kv_offsets, None, p.B, 1,
-                          p.Lq, p.D, p.scale, 0, rows)
-        got = dq[torch.as_tensor(rows, device="cuda"), h]
-        assert parity.rel_l2(got, ref) <= parity.TOL_GRAD, "dQ (batch-summed rows)"
-    del out, lse, dq, dk, dv, p
+        dout = p.dout[os_:oe].cpu()
+        O_ref, L_ref = orc.fwd(q, k, v, kv_sub, q_sub, e - b, H, Lq, D, p.scale)
+        dq_ref, dk_ref, dv_ref = orc.bwd(q, k, v, dout, kv_sub, q_sub, e - b, H, Lq, D, p.scale)
+        O_ref, L_ref = O_ref.numpy(), L_ref.numpy()
+        dq_ref, dk_ref, dv_ref = dq_ref.numpy(), dk_ref.numpy(), dv_ref.numpy()
+        if dq_sum is not None:
+            dq_sum += dq_ref
+        fin = np.isfinite(L_ref)
+        for f, (out, lse, dq, dk, dv) in runs.items():
+            O = out[os_:oe].cpu().double().numpy()
+            L = lse[:, os_:oe].cpu().double().numpy()
+            assert np.isfinite(O).all(), f"flags {f}: O has unwritten or non-finite entries"
+            assert np.array_equal(np.isfinite(L), fin), f"flags {f}: LSE finite pattern differs"
+            if O.size:
+                o_err[f] = max(o_err[f], float(np.abs(O - O_ref).max()))
+            if fin.any():
+                l_err[f] = max(l_err[f], float(np.abs(L[fin] - L_ref[fin]).max()))
+            t = tallies[f]
+            t["dK"].add(dk[ks:ke].cpu().double().numpy(), dk_ref, kv_sub)
+            t["dV"].add(dv[ks:ke].cpu().double().numpy(), dv_ref, kv_sub)
+            if p.mode == "self":
+                t["dQ"].add(dq[qs:qe].cpu().double().numpy(), dq_ref, q_sub)
+    for f, (out, lse, dq, dk, dv) in runs.items():
+        assert o_err[f] <= parity.TOL_O, f"flags {f}: O max-abs error {o_err[f]:.3e}"
+        assert l_err[f] <= parity.TOL_LSE, f"flags {f}: LSE max-abs error {l_err[f]:.3e}"
+        if dq_sum is not None:  # the batch-summed dQ, and each head of it
+            tallies[f]["dQ"].add(dq.cpu().double().numpy(), dq_sum, np.array([0, Lq]))
+        for g in ("dK", "dV", "dQ"):
+            tallies[f][g].check(f"flags {f} {g}")
+    del runs, p
     torch.cuda.empty_cache()

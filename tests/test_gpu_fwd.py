@@ -93,6 +93,43 @@ def test_large_scores_rescale_path():
     _run(p)
 
 
+def test_large_scores_rescale_path_full_scale_v():
+    # The same scores with V at full scale: peaky rows put O near single V
+    # rows, |O| up to about 4, where the 1e-2 max-abs bound on O (which holds
+    # for |O| < 2) no longer does.  The bound derived from the arithmetic:
+    # the PV product uses bf16 weights p~_j = p_j (1 + d_j), |d_j| <= 2^-9, and
+    # O is normalised by their sum, so O_gpu - O is
+    # sum_j w_j (d_j - mean_w d) (V_j - O), at most 2^-8 max_j |V_j - O| per
+    # element; the output's rounding to bf16 adds half an ulp of |O| (2^-8 |O|
+    # for 8 significant bits), and 1e-4 covers the fp32 accumulation and exp2.
+    p = workloads.make_problem(3, 2, 128, "self", [900, 400, 1300], seed=9)
+    ramp = torch.linspace(0.2, 3.0, p.k.shape[0])[:, None, None]
+    p.k = (p.k.float() * ramp).to(torch.bfloat16)
+    p.q = (p.q.float() * 2.0).to(torch.bfloat16)
+    p = parity.to_cuda(p)
+    plan = parity.make_plan(p)
+    out, lse, _ = parity.gpu_fwd(p, plan)
+    O_ref, L_ref = parity.oracle_fwd(p)
+    O = out.cpu().double()
+    assert O_ref.abs().max().item() > 2.0, "the case must reach the |O| >= 2 range"
+    off = p.kv_offsets
+    V = p.v.cpu().double()
+    worst = -1.0
+    for b in range(p.B):
+        s, e = int(off[b]), int(off[b + 1])
+        o, o_ref = O[s:e], O_ref[s:e]                      # [n, H, D] (self mode: q rows = kv rows)
+        vs = V[s:e]
+        spread = torch.maximum(vs.amax(0) - o_ref, o_ref - vs.amin(0))  # max_j |V_j - O_i|
+        mag = torch.maximum(o.abs(), o_ref.abs()).clamp_min(2.0 ** -126)
+        half_ulp = torch.exp2(torch.floor(torch.log2(mag)) - 8)
+        excess = (o - o_ref).abs() - (half_ulp + 2.0 ** -8 * spread + 1e-4)
+        worst = max(worst, excess.max().item())
+    assert worst <= 0.0, f"O error above its bound by {worst:.3e}"
+    assert (lse.cpu().double() - L_ref).abs().max().item() <= parity.TOL_LSE
+    dq, dk, dv = parity.gpu_bwd(p, out, lse, plan)
+    parity.check_grads(dq, dk, dv, *parity.oracle_bwd(p))
+
+
 def test_repeated_calls_are_deterministic():
     p = parity.to_cuda(workloads.make_workload("jagged_self", seed=2))
     plan = parity.make_plan(p)

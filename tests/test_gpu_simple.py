@@ -32,16 +32,19 @@ CASES = {
 
 def _simple(p):
     import jagged_attention_gb300 as jfa
-    out = torch.full((p.n_o_rows, p.H, p.D), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lse = torch.full((p.H, p.n_o_rows), float("nan"), dtype=torch.float32, device="cuda")
+    g = [parity.guarded((p.n_o_rows, p.H, p.D), torch.bfloat16),
+         parity.guarded((p.H, p.n_o_rows), torch.float32),
+         parity.guarded(p.q.shape, torch.float32),
+         parity.guarded(p.k.shape, torch.bfloat16),
+         parity.guarded(p.v.shape, torch.bfloat16)]
+    out, lse, dq, dk, dv = (x.t for x in g)
     jfa.fwd_simple(p.q, p.k, p.v, p.kv_offsets, p.q_offsets, scale=p.scale, out=out, lse=lse)
-    dq = torch.full(p.q.shape, float("nan"), dtype=torch.float32, device="cuda")
-    dk = torch.full(p.k.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
-    dv = torch.full(p.v.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
     jfa.bwd_simple(p.q, p.k, p.v, out, p.dout, lse, p.kv_offsets, p.q_offsets, scale=p.scale,
                    dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     assert jfa.simple_device_status() == 0
+    for x, n in zip(g, ("O", "LSE", "dQ", "dK", "dV")):
+        x.check(n)
     return out, lse, dq, dk, dv
 
 

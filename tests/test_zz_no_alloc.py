@@ -33,18 +33,30 @@ def _entry():
     return fn
 
 
-def _call(fn, p, out, lse, status):
+def _outputs(p):
+    """Guard-banded, NaN-prefilled dQ, dK, dV."""
+    return (parity.guarded(p.q.shape, torch.float32), parity.guarded(p.k.shape, torch.bfloat16),
+            parity.guarded(p.v.shape, torch.bfloat16))
+
+
+def _launch(fn, p, out, lse, status, g):
     kv = jfa._offsets(p.kv_offsets)
     qo = jfa._offsets(p.q_offsets)
-    dq = torch.full(p.q.shape, float("nan"), dtype=torch.float32, device="cuda")
-    dk = torch.full(p.k.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
-    dv = torch.full(p.v.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
-    rc = fn(jfa._i32ptr(kv), jfa._i32ptr(qo), p.B, p.H, p.Lq, p.D, p.q.data_ptr(), p.k.data_ptr(),
-            p.v.data_ptr(), out.data_ptr(), p.dout.data_ptr(), lse.data_ptr(), p.scale,
-            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), status.data_ptr(),
-            torch.cuda.current_stream().cuda_stream)
+    dq, dk, dv = (x.t for x in g)
+    return fn(jfa._i32ptr(kv), jfa._i32ptr(qo), p.B, p.H, p.Lq, p.D, p.q.data_ptr(), p.k.data_ptr(),
+              p.v.data_ptr(), out.data_ptr(), p.dout.data_ptr(), lse.data_ptr(), p.scale,
+              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), status.data_ptr(),
+              torch.cuda.current_stream().cuda_stream)
+
+
+def _call(fn, p, out, lse, status):
+    g = _outputs(p)
+    rc = _launch(fn, p, out, lse, status, g)
     assert rc == 0, jfa.STATUS_NAMES.get(rc, rc)
-    return dq, dk, dv
+    torch.cuda.synchronize()
+    for x, n in zip(g, ("dQ", "dK", "dV")):
+        x.check(n)
+    return tuple(x.t for x in g)
 
 
 CASES = {
@@ -75,6 +87,32 @@ def test_noalloc_matches_jfa_bwd_twice_in_a_row(name):
             assert parity.rel_l2(g, r) <= parity.TOL_GRAD
 
 
+def test_noalloc_matches_the_oracle_and_allocates_nothing():
+    jfa.build()
+    fn = _entry()
+    p = parity.to_cuda(workloads.make_problem(6, 3, 128, "broadcast", [5, 0, 128, 129, 1000, 300],
+                                              Lq=200, seed=41))
+    plan = parity.make_plan(p)
+    out, lse, _ = parity.gpu_fwd(p, plan)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    first = _call(fn, p, out, lse, status)  # sets up the scratch address for this device
+    assert status.item() == 0
+    parity.check_grads(*first, *parity.oracle_bwd(p))
+    # a second call, with its outputs already allocated, must leave the
+    # device's free memory unchanged: nothing is allocated on its behalf
+    g = _outputs(p)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    rc = _launch(fn, p, out, lse, status, g)
+    torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    assert rc == 0 and status.item() == 0
+    assert free_after == free_before, (free_before, free_after)
+    for x, n in zip(g, ("dQ", "dK", "dV")):
+        x.check(n)
+    parity.check_grads(*(x.t for x in g), *parity.oracle_bwd(p))
+
+
 def test_noalloc_needs_no_delta_scratch_when_full_tiles_form_it():
     jfa.build()
     fn = _entry()
@@ -101,14 +139,26 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     jfa.build()
     fn = _entry()
     # 2^20 broadcast rows x 16 heads of Delta (64 MiB) cannot fit the 32 MiB
-    # array: the call must refuse before launching anything (tiny real buffers
-    # stand in for the tensors it never touches).  The sequence has 129 keys,
-    # two key blocks, so Delta needs the scratch (with one key block the tiles
-    # would form it and the call would go ahead).
-    t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
-    f = torch.zeros(16, dtype=torch.float32, device="cuda")
-    kv = jfa._offsets([0, 129])
-    rc = fn(jfa._i32ptr(kv), None, 1, 16, 1 << 20, 64, t.data_ptr(), t.data_ptr(), t.data_ptr(),
-            t.data_ptr(), t.data_ptr(), f.data_ptr(), 0.125, f.data_ptr(), t.data_ptr(),
-            t.data_ptr(), None, torch.cuda.current_stream().cuda_stream)
+    # array: the call must refuse before launching anything.  The sequence has
+    # 129 keys, two key blocks, so Delta needs the scratch (with one key block
+    # the tiles would form it and the call would go ahead).  Every buffer has
+    # the full size the arguments describe (about 10 GiB in all), so that the
+    # call stays within bounds even if the check were ever to let it through.
+    Lq, H, D, nk = 1 << 20, 16, 64, 129
+    q = torch.zeros((Lq, H, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((nk, H, D), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    out = torch.zeros((Lq, H, D), dtype=torch.bfloat16, device="cuda")
+    dout = torch.zeros_like(out)
+    lse = torch.zeros((H, Lq), dtype=torch.float32, device="cuda")
+    dq = torch.zeros((Lq, H, D), dtype=torch.float32, device="cuda")
+    dk = torch.zeros_like(k)
+    dv = torch.zeros_like(k)
+    kv = jfa._offsets([0, nk])
+    rc = fn(jfa._i32ptr(kv), None, 1, H, Lq, D, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+            out.data_ptr(), dout.data_ptr(), lse.data_ptr(), 0.125, dq.data_ptr(), dk.data_ptr(),
+            dv.data_ptr(), None, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
     assert rc == 5  # JFA_ERR_WORKSPACE
+    del q, k, v, out, dout, lse, dq, dk, dv
+    torch.cuda.empty_cache()
