@@ -93,6 +93,26 @@ def packed_runs(prob, pack: bool) -> list:
     return out
 
 
+def packing_applies(prob, mode: str = "auto") -> bool:
+    """Whether the library packs this batch's short sequences: mode "force"
+    (JFA_PLAN_PACK_SHORT) whenever a run forms, "off" (JFA_PLAN_NO_PACK) never,
+    "auto" (no flag) when the runs remove at least an eighth of the forward
+    tiles (a run of n non-empty sequences replaces n one-block tiles by one)."""
+    if mode == "off" or prob.mode == "broadcast":
+        return False
+    runs = packed_runs(prob, True)
+    klen = np.asarray(prob.kv_lengths, dtype=np.int64)
+    saved = sum(int(np.count_nonzero(klen[b:e])) - 1 for b, e in runs)
+    tiles = int(((klen + 127) // 128).sum())
+    return saved > 0 and (mode == "force" or 8 * saved >= tiles)
+
+
+def plan_packs(plan) -> bool:
+    """Whether a plan's forward schedule holds packed tiles (block field < 0)."""
+    tiles, _ = plan.tiles(0)
+    return bool((tiles[:, 2] < 0).any())
+
+
 def dq_rows_cleared(prob, pack: bool) -> int:
     """Query rows whose fp32 dQ the backward pre-pass clears: the library clears
     the rows tiles reduce-add into or never write (all rows in broadcast mode;
@@ -307,6 +327,48 @@ def aggregate_tflops(job_flops_per_step: float, ms_per_step: float) -> float:
     return job_flops_per_step / (ms_per_step * 1e-3) / 1e12
 
 
+# One batch split across ranks (--split-batch, strong scaling): each rank takes
+# a contiguous run of sequences, the runs balanced by the work sum_b Lq_b*Lk_b;
+# the sequences are independent, so only broadcast mode's dQ (every sequence
+# adds into the one shared query block) is summed over the ranks.
+def split_batch(prob, world: int) -> list:
+    """Sequence ranges [b0, b1) of the ranks, cut where the running work crosses
+    r/world of the total (each range non-empty while B >= world)."""
+    work = np.asarray(prob.q_lengths, dtype=np.int64) * np.asarray(prob.kv_lengths, dtype=np.int64)
+    cum = np.concatenate([[0], np.cumsum(work)])
+    cuts = [0]
+    for r in range(1, world):
+        c = int(np.searchsorted(cum, cum[-1] * r / world, side="left"))
+        cuts.append(min(max(c, cuts[-1] + 1), prob.B - (world - r)))
+    cuts.append(prob.B)
+    return [(cuts[r], cuts[r + 1]) for r in range(world)]
+
+
+def shard_problem(prob, b0: int, b1: int):
+    """The sub-problem of sequences [b0, b1): offsets rebased, tensors sliced
+    (views); broadcast mode keeps the whole shared Q."""
+    kvo = prob.kv_offsets.astype(np.int64)
+    ks, ke = int(kvo[b0]), int(kvo[b1])
+    kv_off = (kvo[b0:b1 + 1] - ks).astype(np.int32)
+    if prob.mode == "broadcast":
+        q_off, q = None, prob.q
+        os_, oe = b0 * prob.Lq, b1 * prob.Lq
+    else:
+        qo = prob.q_offsets.astype(np.int64)
+        qs, qe = int(qo[b0]), int(qo[b1])
+        q_off, q = (qo[b0:b1 + 1] - qs).astype(np.int32), prob.q[qs:qe]
+        os_, oe = qs, qe
+    return workloads.Problem(b1 - b0, prob.H, prob.D, prob.mode, prob.Lq, kv_off, q_off, q,
+                             prob.k[ks:ke], prob.v[ks:ke], prob.dout[os_:oe], prob.scale)
+
+
+def reduce_dq(dist, prob, dq):
+    """Broadcast mode: every rank's dQ holds its sequences' share of the one
+    shared query block; the job's dQ is their sum.  Self mode: nothing."""
+    if dist is not None and prob.mode == "broadcast":
+        dist.all_reduce(dq, op=dist.ReduceOp.SUM)
+
+
 # ---------------------------------------------------------------------------
 def run_reference(args, rank, world):
     """The oracle, as it stands, on the host cores (rank 0 only)."""
@@ -353,13 +415,19 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     jfa.lib()
     w = workloads.WORKLOADS[args.workload]
-    prob = workloads.make_workload(args.workload, seed=rank_seed(args.seed, rank), device=dev,
-                                   batch=args.batch)
-    flags = ((jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
-             | (jfa.PLAN_DELTA_PREPASS if args.delta_prepass else 0)
-             | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0))
-    own_delta = tiles_form_delta(prob, args.pack, args.delta_prepass, args.delta_in_tiles)
+    split = args.split_batch and dist is not None
+    if split:  # every rank draws the same batch and keeps its share of the sequences
+        full = workloads.make_workload(args.workload, seed=args.seed, device=dev, batch=args.batch)
+        prob = shard_problem(full, *split_batch(full, world)[rank])
+    else:
+        prob = workloads.make_workload(args.workload, seed=rank_seed(args.seed, rank), device=dev,
+                                       batch=args.batch)
+    flags = plan_flags(args, jfa)
+    pack = packing_applies(prob, pack_mode(args))
+    own_delta = tiles_form_delta(prob, pack, args.delta_prepass, args.delta_in_tiles)
     plan = jfa.Plan(prob.kv_offsets, prob.q_offsets, H=prob.H, D=prob.D, Lq=prob.Lq, flags=flags)
+    if plan_packs(plan) != pack:  # the byte accounting below follows the library's rule
+        raise RuntimeError("bench.py's packing rule disagrees with the library's plan")
     out = torch.empty((prob.n_o_rows, prob.H, prob.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((prob.H, prob.n_o_rows), dtype=torch.float32, device=dev)
     dq = torch.empty(prob.q.shape, dtype=torch.float32, device=dev)
@@ -379,6 +447,8 @@ def run_ours(args, rank, world, dist):
             ev[2].record(stream)
         jfa.bwd_main(plan, prob.q, prob.k, prob.v, prob.dout, lse, prob.scale, dq, dk, dv, ws,
                      stream=stream)
+        if split:
+            reduce_dq(dist, prob, dq)  # NCCL, on the current stream
         if ev is not None:
             ev[3].record(stream)
 
@@ -440,7 +510,7 @@ def run_ours(args, rank, world, dist):
         "jfa_fwd_kernel": {"ms": k_fwd / args.steps, "flops": flops(prob, "fwd"),
                            "bytes": alg_bytes(prob, "fwd"), "src": "fwd.cu"},
         "bwd_preprocess": {"ms": k_pre / args.steps, "flops": 0.0,
-                           "bytes": alg_bytes(prob, "pre", args.pack, own_delta), "src": "bwd.cu"},
+                           "bytes": alg_bytes(prob, "pre", pack, own_delta), "src": "bwd.cu"},
         "jfa_bwd_kernel": {"ms": k_main / args.steps, "flops": flops(prob, "bwd"),
                            "bytes": alg_bytes(prob, "main", own_delta=own_delta), "src": "bwd.cu"},
     }
@@ -482,17 +552,19 @@ def run_ours(args, rank, world, dist):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": args.workload, "B": prob.B, "H": w.H, "D": w.D, "Lq": w.Lq,
+        "higher_is_better": True, "scaling": "strong" if split else "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": full.B if split else prob.B, "H": w.H, "D": w.D,
+                   "Lq": w.Lq,
                    "mode": w.mode, "lengths": list(map(str, w.lengths)), "seed": args.seed,
                    "sum_kv_tokens": int(prob.kv_offsets[-1]),
                    "l2": (f"inputs under twice L2 ({step_input_bytes(prob) / 1e6:.0f} MB per step): "
                           f"a {L2_FLUSH_BYTES >> 20} MiB write flushes L2 before every timed step, "
                           f"outside the step's timed interval") if flush else
                          f"inputs larger than L2 (K+V {kv_gb:.2f} GB per step), no flush",
-                   "parallelism": f"dp{world} (independent batches)",
-                   "plan": ("short sequences packed" if args.pack else "plain schedule")
+                   "parallelism": (f"dp{world} (one batch split by sequence, broadcast dQ all-reduced)"
+                                   if split else f"dp{world} (independent batches)"),
+                   "plan": ("short sequences packed" if pack else "plain schedule")
                            + (", tiles claimed at run time" if args.dynamic else ""),
                    "delta": "formed by the backward tiles" if own_delta else "pre-pass"},
         "fwd_tflops": per_kernel["jfa_fwd_kernel"]["tflops"],
@@ -513,6 +585,17 @@ def run_ours(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def pack_mode(args) -> str:
+    return "force" if args.pack else ("off" if args.no_pack else "auto")
+
+
+def plan_flags(args, jfa) -> int:
+    return ((jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_NO_PACK if args.no_pack else 0)
+            | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
+            | (jfa.PLAN_DELTA_PREPASS if args.delta_prepass else 0)
+            | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0))
+
+
 def run_e2e(args, prob, dev, stream, jfa):
     """Public-API steps with host buffers, as a training loop would run them:
     each step builds a plan from the host offsets, copies its inputs from
@@ -531,9 +614,7 @@ def run_e2e(args, prob, dev, stream, jfa):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * (prob.B + 1) * (
         1 if prob.q_offsets is None else 2)
     d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
-    flags = ((jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
-             | (jfa.PLAN_DELTA_PREPASS if args.delta_prepass else 0)
-             | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0))
+    flags = plan_flags(args, jfa)
     s_in, s_cmp, s_out, s_plan = (torch.cuda.Stream(device=dev) for _ in range(4))
 
     def buffers():
@@ -606,10 +687,16 @@ def main():
                     help="form Delta in the pre-pass even where the backward tiles could (A/B)")
     ap.add_argument("--delta-in-tiles", action="store_true",
                     help="let the backward tiles form Delta wherever they can, whatever their fill")
-    ap.add_argument("--pack", action="store_true",
-                    help="plan with short sequences packed into shared tiles (block-diagonal fast path)")
+    pk = ap.add_mutually_exclusive_group()
+    pk.add_argument("--pack", action="store_true",
+                    help="pack short sequences into shared tiles wherever a run forms (by default "
+                         "the library packs when that removes an eighth of the tiles)")
+    pk.add_argument("--no-pack", action="store_true", help="never pack short sequences")
     ap.add_argument("--batch", type=int, default=None,
                     help="keep only the first B sequences of the workload (profiling captures)")
+    ap.add_argument("--split-batch", action="store_true",
+                    help="under torchrun: split one batch across the ranks by sequence (strong "
+                         "scaling; broadcast mode sums dQ over the ranks) instead of one batch per rank")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -89,18 +89,23 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
 
 /*
  * Plan flags.
- * JFA_PLAN_PACK_SHORT: in self mode with one offsets array shared by queries
- * and keys (q_offsets equal to kv_offsets element by element), runs of
- * consecutive short sequences whose lengths add up to at most 128 rows (with
- * at least two non-empty ones) share one 128-row tile, masked block-diagonally
- * so every row still sees only its own sequence.  This is the block-diagonal
- * case of the TLX Block Attention page ("One Constraint, Five Eliminations":
- * each query tile meets exactly one key tile), which the plain schedule runs
- * at half occupancy when segments are shorter than a tile.  Such a tile is
- * recorded as {b0, h, -nseq, 1}.  Ignored in broadcast mode or when the
- * offsets differ.
+ * Packing of short sequences: in self mode with one offsets array shared by
+ * queries and keys (q_offsets equal to kv_offsets element by element), runs
+ * of consecutive short sequences whose lengths add up to at most 128 rows
+ * (with at least two non-empty ones) share one 128-row tile, masked
+ * block-diagonally so every row still sees only its own sequence.  This is
+ * the block-diagonal case of the TLX Block Attention page ("One Constraint,
+ * Five Eliminations": each query tile meets exactly one key tile), which an
+ * unpacked schedule runs at half occupancy when segments are shorter than a
+ * tile.  Such a tile is recorded as {b0, h, -nseq, 1}.  Never in broadcast
+ * mode or when the offsets differ.  By default a plan packs when that removes
+ * at least an eighth of its forward tiles (a pack of n non-empty sequences
+ * replaces n tiles by one).
+ * JFA_PLAN_PACK_SHORT: pack whenever a run forms.
+ * JFA_PLAN_NO_PACK: never pack.  Setting both is JFA_ERR_INVALID_ARG.
  */
 #define JFA_PLAN_PACK_SHORT 1u
+#define JFA_PLAN_NO_PACK 32u
 
 /*
  * JFA_PLAN_DYNAMIC: tiles are claimed at run time instead of dealt on the

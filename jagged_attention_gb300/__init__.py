@@ -32,6 +32,7 @@ PLAN_PACK_SHORT = 1  # JFA_PLAN_PACK_SHORT
 PLAN_DYNAMIC = 2  # JFA_PLAN_DYNAMIC
 PLAN_DELTA_PREPASS = 4  # JFA_PLAN_DELTA_PREPASS
 PLAN_DELTA_IN_TILES = 8  # JFA_PLAN_DELTA_IN_TILES
+PLAN_NO_PACK = 32  # JFA_PLAN_NO_PACK
 
 
 class JfaError(RuntimeError):

@@ -144,10 +144,29 @@ bool tiles_form_delta(unsigned flags, const std::vector<int64_t>& qlen,
   return (flags & JFA_PLAN_DELTA_IN_TILES) || mean_tile_keys(bwd, kv_off) >= 96.0;
 }
 
-// Packing needs self mode with one offsets array for queries and keys.
-bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B) {
-  if (!(flags & JFA_PLAN_PACK_SHORT) || !q_off) return false;
-  return std::memcmp(kv_off, q_off, (B + 1) * sizeof(int32_t)) == 0;
+// Whether the plan packs short sequences, and the packing (pack[b] as
+// short_packs gives it) when it does.  Packing needs self mode with one
+// offsets array for queries and keys.  JFA_PLAN_PACK_SHORT packs whenever a
+// run forms, JFA_PLAN_NO_PACK never; by default a plan packs when that
+// removes at least an eighth of its forward tiles (a pack of n non-empty
+// sequences replaces n one-block tiles by one).
+bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B,
+                 const std::vector<int64_t>& kvlen, std::vector<int>* pack) {
+  if ((flags & JFA_PLAN_NO_PACK) || !q_off) return false;
+  if (std::memcmp(kv_off, q_off, (B + 1) * sizeof(int32_t)) != 0) return false;
+  std::vector<int> p = jfa::short_packs(kvlen);
+  int64_t saved = 0, tiles = 0;
+  for (int b = 0; b < B; ++b) {
+    tiles += (kvlen[b] + jfa::kBM - 1) / jfa::kBM;
+    if (p[b] > 1) {
+      int64_t nonempty = 0;
+      for (int i = b; i < b + p[b]; ++i) nonempty += kvlen[i] > 0;
+      saved += nonempty - 1;
+    }
+  }
+  if (saved == 0 || (!(flags & JFA_PLAN_PACK_SHORT) && 8 * saved < tiles)) return false;
+  *pack = std::move(p);
+  return true;
 }
 
 }  // namespace
@@ -173,13 +192,13 @@ int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
                     int32_t* cta_ptr_out, int* T, int* P) {
   if (!kv_offsets_host || B < 1 || H < 1 || num_ctas < 1 || (dir != 0 && dir != 1) || !T || !P)
     return JFA_ERR_INVALID_ARG;
+  if ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) return JFA_ERR_INVALID_ARG;
   std::vector<int64_t> qlen, kvlen;
   int64_t n_kv = 0, n_q = 0;
   int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
   if (rc != JFA_OK) return rc;
   std::vector<int> pack;
-  const bool packing = use_packing(flags, kv_offsets_host, q_offsets_host, B);
-  if (packing) pack = jfa::short_packs(kvlen);
+  const bool packing = use_packing(flags, kv_offsets_host, q_offsets_host, B, kvlen, &pack);
   const bool dyn = (flags & JFA_PLAN_DYNAMIC) != 0;
   const Schedule s =
       dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, dyn)
@@ -195,13 +214,13 @@ int jfa_delta_in_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_
                        int Lq, unsigned flags, int* in_tiles) {
   if (!kv_offsets_host || B < 1 || !in_tiles) return JFA_ERR_INVALID_ARG;
   if ((flags & JFA_PLAN_DELTA_PREPASS) && (flags & JFA_PLAN_DELTA_IN_TILES)) return JFA_ERR_INVALID_ARG;
+  if ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) return JFA_ERR_INVALID_ARG;
   std::vector<int64_t> qlen, kvlen;
   int64_t n_kv = 0, n_q = 0;
   int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
   if (rc != JFA_OK) return rc;
   std::vector<int> pack;
-  const bool packing = use_packing(flags, kv_offsets_host, q_offsets_host, B);
-  if (packing) pack = jfa::short_packs(kvlen);
+  const bool packing = use_packing(flags, kv_offsets_host, q_offsets_host, B, kvlen, &pack);
   // the mean tile fill does not depend on the head count or the CTA count
   const Schedule s = jfa::build_bwd_schedule(qlen, kvlen, 1, 1, packing ? &pack : nullptr, false);
   *in_tiles = tiles_form_delta(flags, qlen, kvlen, s, kv_offsets_host) ? 1 : 0;
@@ -218,6 +237,7 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   if (!out || !kv_offsets_host || B < 1 || H < 1 || num_ctas < 0) return JFA_ERR_INVALID_ARG;
   *out = nullptr;
   if ((flags & JFA_PLAN_DELTA_PREPASS) && (flags & JFA_PLAN_DELTA_IN_TILES)) return JFA_ERR_INVALID_ARG;
+  if ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) return JFA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
   std::vector<int64_t> qlen, kvlen;
   int64_t n_kv = 0, n_q = 0;
@@ -247,8 +267,7 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   p->n_o = n_o;
   p->n_kv = n_kv;
   std::vector<int> pack;
-  p->packed = use_packing(flags, kv_offsets_host, q_offsets_host, B);
-  if (p->packed) pack = jfa::short_packs(kvlen);
+  p->packed = use_packing(flags, kv_offsets_host, q_offsets_host, B, kvlen, &pack);
   if (!q_offsets_host) {
     if (n_q > 0) p->dq_rows_to_clear.emplace_back(0, n_q);
   } else {

@@ -809,13 +809,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& q, const CUtensorM
   using C = BwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static_assert(sizeof(BwdBars) <= C::kBarBytes, "barrier block");
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(jfa_bwd_kernel<D, kPack, kSelf, kDyn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = set_smem_limit_once<jfa_bwd_kernel<D, kPack, kSelf, kDyn>>(C::kSmemBytes);
+  if (e != cudaSuccess) return e;
   jfa_bwd_kernel<D, kPack, kSelf, kDyn><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dO, dq, dk, dv, a);
   return cudaGetLastError();
 }
@@ -838,7 +833,12 @@ cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta
                          int H, int D, cudaStream_t stream) {
   const int64_t threads = n_o * H * (D / 8);
   if (threads == 0) return cudaSuccess;
-  const int64_t blocks = std::min<int64_t>((threads + 255) / 256, int64_t(152) * 64);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // a grid-stride loop over enough blocks to fill every SM of this device
+  const int64_t blocks = std::min<int64_t>((threads + 255) / 256, int64_t(sms) * 64);
   delta_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(out, dout, delta, n_o, H, D);
   return cudaGetLastError();
 }

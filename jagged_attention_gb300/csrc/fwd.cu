@@ -522,13 +522,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorM
   using C = FwdCfg<D>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static_assert(sizeof(FwdBars) <= C::kBarBytes, "barrier block");
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(jfa_fwd_kernel<D, kPack, kDyn>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = set_smem_limit_once<jfa_fwd_kernel<D, kPack, kDyn>>(C::kSmemBytes);
+  if (e != cudaSuccess) return e;
   jfa_fwd_kernel<D, kPack, kDyn><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, o, a);
   return cudaGetLastError();
 }

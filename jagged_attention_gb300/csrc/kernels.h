@@ -1,10 +1,26 @@
 // kernels.h -- parameter blocks and launchers of the device kernels (internal).
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace jfa {
+
+// The dynamic shared-memory limit of kernel K raised to `bytes`, once for
+// each device the process launches it on (the attribute is per device).
+template <auto K>
+cudaError_t set_smem_limit_once(int bytes) {
+  static std::atomic<uint64_t> done{0};  // bit d: device d configured
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Problem description shared by every kernel.  Offsets are device int32
 // [B+1]; q_off == nullptr selects broadcast mode (Q has Lq rows shared by all

@@ -30,7 +30,8 @@ def test_binding_constants_match_the_header():
     text = jfa.HEADER.read_text()
     flags = {m[0]: int(m[1]) for m in re.findall(r"#define JFA_PLAN_(\w+) (\d+)u", text)}
     assert flags == {"PACK_SHORT": jfa.PLAN_PACK_SHORT, "DYNAMIC": jfa.PLAN_DYNAMIC,
-                     "DELTA_PREPASS": jfa.PLAN_DELTA_PREPASS, "DELTA_IN_TILES": jfa.PLAN_DELTA_IN_TILES}
+                     "DELTA_PREPASS": jfa.PLAN_DELTA_PREPASS, "DELTA_IN_TILES": jfa.PLAN_DELTA_IN_TILES,
+                     "NO_PACK": jfa.PLAN_NO_PACK}
     codes = {int(m[1]): m[0] for m in re.findall(r"\b(JFA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text)}
     assert codes == jfa.STATUS_NAMES
 
@@ -99,8 +100,13 @@ def test_native_builder_matches_reference_on_workloads(name):
     else:
         qlen, qo, Lq = klen, kv, 0
     for d in (0, 1):
-        t, p = jfa.build_tiles(kv, qo, H=w.H, Lq=Lq, num_ctas=152, direction=d)
+        t, p = jfa.build_tiles(kv, qo, H=w.H, Lq=Lq, num_ctas=152, direction=d, flags=jfa.PLAN_NO_PACK)
         rt, rp = _ref(qlen, klen, w.H, 152, d)
+        assert np.array_equal(t, rt) and np.array_equal(p, rp)
+        # the default plan: packed where the default rule says so
+        t, p = jfa.build_tiles(kv, qo, H=w.H, Lq=Lq, num_ctas=152, direction=d)
+        pack = ref_tiles.short_packs(klen) if qo is not None and _auto_packs(klen) else None
+        rt, rp = _ref(qlen, klen, w.H, 152, d, pack)
         assert np.array_equal(t, rt) and np.array_equal(p, rp)
 
 
@@ -128,7 +134,7 @@ def test_native_packed_builder_matches_reference_random(seed):
 def test_packed_block_diagonal_workload_halves_the_tiles():
     w = workloads.WORKLOADS["block_diag"]
     kv = workloads.offsets_from_lengths(workloads.draw_lengths(w.lengths, w.B, 0))
-    plain = jfa.build_tiles(kv, kv, H=w.H, num_ctas=152, direction=0)[0]
+    plain = jfa.build_tiles(kv, kv, H=w.H, num_ctas=152, direction=0, flags=jfa.PLAN_NO_PACK)[0]
     packed = jfa.build_tiles(kv, kv, H=w.H, num_ctas=152, direction=0, flags=jfa.PLAN_PACK_SHORT)[0]
     assert packed.shape[0] * 2 == plain.shape[0]
     assert (packed[:, 2] == -2).all() and (packed[:, 3] == 1).all()
@@ -142,8 +148,9 @@ def test_seed0_tile_counts():
         w = workloads.WORKLOADS[name]
         kv = workloads.offsets_from_lengths(workloads.draw_lengths(w.lengths, w.B, 0))
         qo = None if w.mode == "broadcast" else kv
-        assert jfa.build_tiles(kv, qo, H=w.H, Lq=w.Lq, num_ctas=152, direction=0)[0].shape[0] == tf
-        assert jfa.build_tiles(kv, qo, H=w.H, Lq=w.Lq, num_ctas=152, direction=1)[0].shape[0] == tb
+        nopack = jfa.PLAN_NO_PACK  # the unpacked schedule the quoted totals count
+        assert jfa.build_tiles(kv, qo, H=w.H, Lq=w.Lq, num_ctas=152, direction=0, flags=nopack)[0].shape[0] == tf
+        assert jfa.build_tiles(kv, qo, H=w.H, Lq=w.Lq, num_ctas=152, direction=1, flags=nopack)[0].shape[0] == tb
 
 
 def _create(kv, qo, B, H, Lq, D, num_ctas=0, flags=0):
@@ -200,6 +207,16 @@ def test_rejects_bad_arguments_before_touching_the_device():
     assert L.jfa_simple_release() == 0
 
 
+def _auto_packs(klen):
+    """The default packing rule restated: the reference packer's runs remove at
+    least an eighth of the forward tiles (one tile per non-empty sequence of up
+    to 128 rows, a run of n of them one tile)."""
+    klen = np.asarray(klen, dtype=np.int64)
+    runs = ref_tiles.short_packs(klen)
+    saved = sum(int(np.count_nonzero(klen[b:b + n])) - 1 for b, n in enumerate(runs) if n > 1)
+    return saved > 0 and 8 * saved >= int(((klen + 127) // 128).sum())
+
+
 def _rule(klen, qlen, pack):
     """The documented rule, restated from the lengths alone: every sequence with
     queries has at most 128 keys, and the backward tiles (one per such
@@ -239,6 +256,13 @@ def test_noalloc_refuses_what_a_plan_refuses_before_touching_the_device():
     assert fn(*args(0, 64)) == 1         # no heads: JFA_ERR_INVALID_ARG
 
 
+def test_packing_flags_are_exclusive():
+    kv = np.array([0, 30, 60], dtype=np.int32)
+    with pytest.raises(jfa.JfaError):
+        jfa.build_tiles(kv, kv, H=1, num_ctas=2, direction=0,
+                        flags=jfa.PLAN_PACK_SHORT | jfa.PLAN_NO_PACK)
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_delta_path_follows_the_documented_rule(seed):
     rng = np.random.default_rng(seed)
@@ -247,8 +271,7 @@ def test_delta_path_follows_the_documented_rule(seed):
         hi = int(rng.choice([64, 128, 129, 300]))
         klen = rng.integers(0, hi + 1, B)
         kv = np.concatenate([[0], np.cumsum(klen)]).astype(np.int32)
-        for pack in (False, True):
-            flags = jfa.PLAN_PACK_SHORT if pack else 0
+        for flags, pack in ((jfa.PLAN_NO_PACK, False), (jfa.PLAN_PACK_SHORT, True), (0, _auto_packs(klen))):
             want = _rule(klen, klen, pack)
             assert jfa.delta_in_tiles(kv, kv, flags=flags) == want
             assert jfa.delta_in_tiles(kv, kv, flags=flags | jfa.PLAN_DELTA_PREPASS) is False
@@ -262,18 +285,20 @@ def test_delta_path_on_the_workloads():
     # agree on every workload (lengths only: no tensors are drawn)
     import types
     import bench
-    cases = {("tiny_broadcast", False): False, ("jagged_self", False): False,
-             ("gem_broadcast", False): False, ("block_diag", False): False,
-             ("block_diag", True): True}
-    for (name, pack), want in cases.items():
+    mode_flags = {"auto": 0, "force": jfa.PLAN_PACK_SHORT, "off": jfa.PLAN_NO_PACK}
+    cases = {("tiny_broadcast", "auto"): False, ("jagged_self", "auto"): False,
+             ("gem_broadcast", "auto"): False, ("block_diag", "off"): False,
+             ("block_diag", "auto"): True, ("block_diag", "force"): True}
+    for (name, mode), want in cases.items():
         w = workloads.WORKLOADS[name]
         klen = workloads.draw_lengths(w.lengths, w.B, 0)
         kv = workloads.offsets_from_lengths(klen)
         qlen = np.full(w.B, w.Lq) if w.mode == "broadcast" else klen
         qo = None if w.mode == "broadcast" else kv
-        got = jfa.delta_in_tiles(kv, qo, Lq=w.Lq, flags=jfa.PLAN_PACK_SHORT if pack else 0)
+        got = jfa.delta_in_tiles(kv, qo, Lq=w.Lq, flags=mode_flags[mode])
         prob = types.SimpleNamespace(kv_lengths=klen, q_lengths=qlen, mode=w.mode)
-        assert got == want == bench.tiles_form_delta(prob, pack), name
+        pack = bench.packing_applies(prob, mode)
+        assert got == want == bench.tiles_form_delta(prob, pack), (name, mode)
     with pytest.raises(jfa.JfaError):
         jfa.delta_in_tiles([0, 5], None, Lq=4, flags=jfa.PLAN_DELTA_PREPASS | jfa.PLAN_DELTA_IN_TILES)
 
@@ -291,6 +316,12 @@ def test_bench_packing_matches_the_reference_packer(seed):
         want = [(b, b + n) for b, n in enumerate(pack) if n > 1]
         assert bench.packed_runs(prob, True) == want
         assert bench.packed_runs(prob, False) == []
+        # the benchmark's copy of the default rule agrees with the library's plans
+        kv = np.concatenate([[0], np.cumsum(klen)]).astype(np.int32)
+        for mode, flags in (("auto", 0), ("force", jfa.PLAN_PACK_SHORT), ("off", jfa.PLAN_NO_PACK)):
+            tiles = jfa.build_tiles(kv, kv, H=1, num_ctas=4, direction=0, flags=flags)[0]
+            assert bench.packing_applies(prob, mode) == bool((tiles[:, 2] < 0).any()), (mode, klen)
+        assert bench.packing_applies(prob, "auto") == _auto_packs(klen)
 
 
 def test_bench_flushes_l2_only_for_small_workloads():

@@ -34,7 +34,8 @@ pytestmark = pytest.mark.gpu
 VARIANTS = {
     "gem_broadcast": [0, jfa.PLAN_DYNAMIC],
     "skewed_broadcast": [0],
-    "block_diag": [0, jfa.PLAN_PACK_SHORT, jfa.PLAN_PACK_SHORT | jfa.PLAN_DYNAMIC],
+    # unpacked, packed by the default rule, packed with dynamic claiming
+    "block_diag": [jfa.PLAN_NO_PACK, 0, jfa.PLAN_DYNAMIC],
 }
 CHUNK_KV_ROWS = 1 << 17
 LOCAL_TOL = 2e-2

@@ -46,7 +46,8 @@ def _case(i):
         p = workloads.make_problem(B, H, D, "self", klen.tolist(), q_lengths=qlen.tolist(), seed=2000 + i)
     else:
         p = workloads.make_problem(B, H, D, "self", klen.tolist(), seed=2000 + i)
-    flags = int(rng.integers(0, 4))  # bit 0 packing (self mode only), bit 1 dynamic tiles
+    # packing (self mode only): forced, off or the default rule; dynamic tiles or not
+    flags = int(rng.choice([1, 32, 0])) | (2 if rng.integers(0, 2) else 0)
     num_ctas = int(rng.choice([0, 1, 2, 5, 17]))
     return p, flags, num_ctas
 

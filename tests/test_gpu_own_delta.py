@@ -51,7 +51,7 @@ def _in_tiles():
     return jfa.PLAN_DELTA_IN_TILES
 
 
-@pytest.mark.parametrize("flags", [0, 1, 2])  # plain, PLAN_PACK_SHORT, PLAN_DYNAMIC
+@pytest.mark.parametrize("flags", [32, 1, 34])  # PLAN_NO_PACK, PLAN_PACK_SHORT, PLAN_DYNAMIC | PLAN_NO_PACK
 @pytest.mark.parametrize("case", sorted(CASES))
 @pytest.mark.parametrize("D", [64, 128])
 def test_in_kernel_delta_matches_oracle(D, case, flags):
@@ -101,7 +101,8 @@ def test_default_rule_full_tiles_form_delta():
 
 
 def test_default_rule_half_full_tiles_keep_the_prepass():
-    # the same segments one per tile: 64 key rows per tile
+    # the same segments one per tile (packing turned off): 64 key rows per tile
+    import jagged_attention_gb300 as jfa
     p = parity.to_cuda(workloads.make_problem(24, 2, 128, "self", [64] * 24, seed=35))
-    _, dk, _ = _grads(p, poison_out=True)
+    _, dk, _ = _grads(p, jfa.PLAN_NO_PACK, poison_out=True)
     assert torch.isnan(dk.float()).any()
