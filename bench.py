@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # 256-sequence capture of the same kernel, scaled by K/V tokens: x3.730),
 # keyed by kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2518e+09, "src_hash": "120f0edaa62c677d"},
-    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7859e+09, "src_hash": "ac59d5daa306ef69"},
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2559e+09, "src_hash": "bcfe3c17d7a8944e"},
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7861e+09, "src_hash": "90ee7b645f18074f"},
 }
 
 
