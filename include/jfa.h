@@ -140,6 +140,25 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
 #define JFA_PLAN_DELTA_PREPASS 4u
 #define JFA_PLAN_DELTA_IN_TILES 8u
 
+/*
+ * JFA_PLAN_FWD_PAIRS: run the forward as CTA pairs where the pair kernel
+ * applies (D = 128, static schedule, no packed tiles, num_ctas >= 2).  Two
+ * CTAs of a thread-block cluster take the two query blocks of a "pair tile"
+ * (b, h, mp) -- query rows [256 mp, 256 mp + 256) of sequence b; a sequence
+ * with an odd number of query blocks leaves its last pair tile half empty --
+ * and share every K/V block, each loading half of it; one thread issues the
+ * pair's tensor-core products, which span both CTAs' query rows (M = 256)
+ * and so cost the pair fewer instructions than two single-CTA tiles (the
+ * pages' 2-CTA collaborative MMA: alphasignal JFA page, "Five changes
+ * unlocked the gains", closing paragraph).  The forward schedule then lists
+ * pair tiles {b, h, mp, cost} over P = min(num_ctas / 2, T) pairs.
+ * Without the flag a plan runs one CTA per query block: on GB300 that form
+ * measures faster on every workload tried (the pair's K/V loads, half per
+ * CTA plus the peer's half over the pair, arrive no sooner than a single
+ * CTA's whole block, and its query blocks share no K/V through L2).
+ */
+#define JFA_PLAN_FWD_PAIRS 64u
+
 /* jfa_plan_create with flags (0 = the schedule described above). */
 int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                        int Lq, int D, int num_ctas, unsigned flags, void* stream, jfa_plan_t* out);
@@ -148,20 +167,28 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
 int jfa_plan_destroy(jfa_plan_t plan);
 
 /*
- * Copy a plan's tile schedule to host memory.  dir: 0 forward, 1 backward.
+ * Copy a plan's tile schedule to host memory.  dir: 0 forward (the schedule
+ * the plan launches: over pair tiles when it runs CTA pairs, see
+ * jfa_plan_forward_pairs), 1 backward.
  * tiles_host receives T records of four int32 {b, h, block, cost} grouped by
- * CTA, cta_ptr_host receives P+1 CSR offsets (P = min(num_ctas, T)).  Either
+ * CTA (or pair), cta_ptr_host receives P+1 CSR offsets (P = min(num_ctas, T),
+ * or the number of pairs).  Either
  * buffer may be NULL to query only *T and *P.  Buffers must hold 4*T and P+1
  * int32.
  */
 int jfa_plan_tiles(jfa_plan_t plan, int dir, int32_t* tiles_host, int32_t* cta_ptr_host, int* T,
                    int* P);
 
+/* *pairs = 1 when the plan's forward runs as CTA pairs (JFA_PLAN_FWD_PAIRS), else 0. */
+int jfa_plan_forward_pairs(jfa_plan_t plan, int* pairs);
+
 /*
  * Host-only schedule builder (no GPU needed): the same lists a plan created
- * with the same flags holds.  q_offsets_host == NULL means broadcast with Lq
- * rows.  Call once with tiles_out == NULL to learn *T and *P, then with
- * buffers of 4*T and P+1 int32.
+ * with the same flags holds.  dir: 0 forward (one CTA per query block), 1
+ * backward, 2 forward over pair tiles (num_ctas then counts CTA pairs).
+ * q_offsets_host == NULL means broadcast with Lq rows.  Call once with
+ * tiles_out == NULL to learn *T and *P, then with buffers of 4*T and P+1
+ * int32.
  */
 int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                     int Lq, int num_ctas, int dir, unsigned flags, int32_t* tiles_out,

@@ -150,6 +150,27 @@ bool tiles_form_delta(unsigned flags, const std::vector<int64_t>& qlen,
 // run forms, JFA_PLAN_NO_PACK never; by default a plan packs when that
 // removes at least an eighth of its forward tiles (a pack of n non-empty
 // sequences replaces n one-block tiles by one).
+// Whether the forward runs as CTA pairs (two CTAs of a cluster take the two
+// query blocks of a pair tile and share each K/V block, the tensor-core
+// products spanning both: cta_group::2): on request, where the pair kernel
+// exists (D = 128, static schedule, no packed tiles) and there are queries.
+bool use_fwd_pairs(unsigned flags, int D, bool packed, bool dynamic, int num_ctas,
+                   const std::vector<int64_t>& qlen) {
+  if (!(flags & JFA_PLAN_FWD_PAIRS) || D != 128 || packed || dynamic || num_ctas < 2) return false;
+  for (const int64_t q : qlen)
+    if (q > 0) return true;
+  return false;
+}
+
+// Query lengths in units of pair tiles: the forward schedule over query
+// blocks of 2 * 128 rows is the one over blocks of 128 rows of half-length
+// sequences (ceil(ceil(q / 128) / 2) = ceil(ceil(q / 2) / 128)).
+std::vector<int64_t> pair_lengths(const std::vector<int64_t>& qlen) {
+  std::vector<int64_t> h(qlen.size());
+  for (size_t b = 0; b < qlen.size(); ++b) h[b] = (qlen[b] + 1) / 2;
+  return h;
+}
+
 bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B,
                  const std::vector<int64_t>& kvlen, std::vector<int>* pack) {
   if ((flags & JFA_PLAN_NO_PACK) || !q_off) return false;
@@ -190,7 +211,7 @@ const char* jfa_status_string(int s) {
 int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                     int Lq, int num_ctas, int dir, unsigned flags, int32_t* tiles_out,
                     int32_t* cta_ptr_out, int* T, int* P) {
-  if (!kv_offsets_host || B < 1 || H < 1 || num_ctas < 1 || (dir != 0 && dir != 1) || !T || !P)
+  if (!kv_offsets_host || B < 1 || H < 1 || num_ctas < 1 || dir < 0 || dir > 2 || !T || !P)
     return JFA_ERR_INVALID_ARG;
   if ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) return JFA_ERR_INVALID_ARG;
   std::vector<int64_t> qlen, kvlen;
@@ -202,7 +223,8 @@ int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
   const bool dyn = (flags & JFA_PLAN_DYNAMIC) != 0;
   const Schedule s =
       dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, dyn)
-               : jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, dyn);
+      : dir == 1 ? jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, dyn)
+                 : jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, num_ctas, nullptr, false);
   *T = s.T;
   *P = s.P;
   if (tiles_out) std::memcpy(tiles_out, s.tiles.data(), s.tiles.size() * sizeof(int32_t));
@@ -293,7 +315,10 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
     }
   }
   p->dynamic = (flags & JFA_PLAN_DYNAMIC) != 0;
-  p->fwd = jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->dynamic);
+  p->fwd_pair = use_fwd_pairs(flags, D, p->packed, p->dynamic, p->num_ctas, qlen);
+  p->fwd = p->fwd_pair ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas / 2, nullptr, false)
+                       : jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr,
+                                                 p->dynamic);
   p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->dynamic);
   p->own_delta = tiles_form_delta(flags, qlen, kvlen, p->bwd, kv_offsets_host);
   for (int b = 0; b < B; ++b) {
@@ -356,6 +381,12 @@ int jfa_plan_destroy(jfa_plan_t plan) {
   return rc;
 }
 
+int jfa_plan_forward_pairs(jfa_plan_t plan, int* pairs) {
+  if (!plan || !pairs) return JFA_ERR_INVALID_ARG;
+  *pairs = plan->fwd_pair ? 1 : 0;
+  return JFA_OK;
+}
+
 int jfa_plan_selftest(jfa_plan_t plan, int skip, unsigned limit_us) {
   if (!plan || skip < 0 || skip > 2 || limit_us > 2000000u) return JFA_ERR_INVALID_ARG;
   plan->test_skip = skip;
@@ -399,7 +430,8 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
   if (plan->fwd.P == 0) return JFA_OK;
   const int64_t cols = int64_t(plan->H) * plan->D;
   CUtensorMap qm, km, vm, om;
-  if (make_map(&qm, q, plan->n_q, cols) || make_map(&km, k, plan->n_kv, cols) ||
+  // a CTA of a pair loads 64-row halves of each K block
+  if (make_map(&qm, q, plan->n_q, cols) || make_map(&km, k, plan->n_kv, cols, plan->fwd_pair ? 64 : 128) ||
       make_map(&vm, v, plan->n_kv, cols) || make_map(&om, out, plan->n_o, cols, 32))
     return JFA_ERR_CUDA;
   jfa::FwdArgs a;
@@ -419,7 +451,9 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
     if (cudaMemsetAsync(a.dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return JFA_ERR_CUDA;
   }
-  cudaError_t e = jfa::launch_fwd(a, qm, km, vm, om, plan->fwd.P, static_cast<cudaStream_t>(stream));
+  a.pair = plan->fwd_pair;
+  cudaError_t e = jfa::launch_fwd(a, qm, km, vm, om, plan->fwd_pair ? 2 * plan->fwd.P : plan->fwd.P,
+                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

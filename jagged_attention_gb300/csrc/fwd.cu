@@ -27,6 +27,8 @@
 // more than 2^8 (the stale max keeps every P <= 256, exact after the final
 // division by l).  The last, partial key block is the only one that masks
 // (the pages' "loop peeling": the bulk pass is branch-free).
+#include <type_traits>
+
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 #include "tiles.cuh"
@@ -37,19 +39,29 @@ namespace {
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+// kPair: a CTA of a pair (the 2-CTA form below) holds half of each K/V
+// block: K rows [64 r, 64 r + 64) of the block with all D columns, and V's
+// 64 columns [64 r, 64 r + 64) of all 128 rows (r = the CTA's rank).
+template <int D, bool kPair = false>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;             // 128-byte column chunks per row
   static constexpr int kChunkBytes = 128 * 128;      // one [128 rows x 64 bf16] chunk
   static constexpr int kTileBytes = 128 * D * 2;     // one 128-row tile of Q, K or V
-  static constexpr int kStages = (D == 128) ? 2 : 4; // K and V ring depth (keeps 1 CTA/SM)
+  static constexpr int kStages = kPair ? 4 : (D == 128) ? 2 : 4;  // K and V ring depth (keeps 1 CTA/SM)
+  static constexpr int kKChunkBytes = kPair ? 64 * 128 : kChunkBytes;  // one 64-column chunk of K
+  static constexpr int kKBytes = kPair ? 64 * D * 2 : kTileBytes;      // a K stage
+  // K/V blocks the L2 prefetch runs ahead of the loads: the pair's ring
+  // waits on load latency (two blocks ahead measured best); one CTA per
+  // block is faster without it
+  static constexpr int kPrefetch = kPair ? 2 : 0;
+  static constexpr int kVBytes = kPair ? 128 * 64 * 2 : kTileBytes;    // a V stage
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kKBytes;
   // row statistics the two softmax groups exchange: per-block partial maxima
   // (2 buffers x 2 groups x 128 rows) and per-tile partial sums (2 buffers x
   // 2 groups x 2 sums x 128 rows)
-  static constexpr int kOffXMax = kOffV + kStages * kTileBytes;
+  static constexpr int kOffXMax = kOffV + kStages * kVBytes;
   static constexpr int kOffXSum = kOffXMax + 2 * 2 * 128 * 4;
   // O leaves through shared memory at D = 128: per softmax group a
   // 128-byte-swizzled [128 rows x 64 bf16] box, stored by TMA a warp (32
@@ -70,6 +82,8 @@ struct FwdCfg {
 struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  // CTA pairs, in the even CTA: the odd CTA's loads of the same stages
+  uint64_t q_pair, k_pair[4], v_pair[4];
   uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
   uint64_t o_empty;
   // per buffer and TMEM lane quadrant (the two warps, one per group, that
@@ -108,23 +122,61 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
-template <int D, bool kPack, class Seq>
+// CTA pairs (kPair): both CTAs of a pair walk the same pair tiles
+// {b, h, mp, cost}; CTA r takes query block 2 mp + r and loads its half of
+// every K/V block (see FwdCfg).
+template <int D, bool kPack, bool kPair, class Seq>
 __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const CUtensorMap* k_map,
                              const CUtensorMap* v_map, uint32_t sbase, FwdBars& bars,
-                             const Abort& ab, Seq& seq) {
-  using C = FwdCfg<D>;
+                             const Abort& ab, Seq& seq, uint32_t rank) {
+  using C = FwdCfg<D, kPair>;
   tma_prefetch_desc(q_map);
   tma_prefetch_desc(k_map);
   tma_prefetch_desc(v_map);
   const uint32_t sQ = sbase + C::kOffQ;
   uint32_t nq = 0, nk = 0, nv = 0;  // loads issued
   bool ok = true;
+  // L2 prefetch cursor (static schedules): walks this CTA's blocks, across
+  // tile boundaries, kPrefetch blocks ahead of the K loads, so that DRAM
+  // reads start earlier than the shared-memory ring alone would let them
+  [[maybe_unused]] int pf_i = 0, pf_end = 0, pf_j = 0;
+  [[maybe_unused]] uint32_t npf = 0;
+  constexpr bool kStatic = std::is_same_v<Seq, TileSeq<false>>;
+  if constexpr (kStatic) {
+    pf_i = seq.i;
+    pf_end = seq.end;
+  }
+  auto prefetch_to = [&](uint32_t target) {
+    if constexpr (kStatic && C::kPrefetch > 0) {
+      while (npf < target && pf_i < pf_end) {
+        const Tile u = load_tile(a.tiles, pf_i);
+        if (pf_j >= u.cost) {
+          ++pf_i;
+          pf_j = 0;
+          continue;
+        }
+        const int y = a.pb.kv_off[u.b] + pf_j * 128, x = u.h * D;
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_prefetch_l2_2d(k_map, x + c * 64, y + (kPair ? 64 * int(rank) : 0));
+        if constexpr (kPair) {
+          tma_prefetch_l2_2d(v_map, x + 64 * int(rank), y);
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c) tma_prefetch_l2_2d(v_map, x + c * 64, y);
+        }
+        ++pf_j;
+        ++npf;
+      }
+    }
+  };
   auto next = [&] { return seq.claim(a.dyn_counter, a.T, bars.ring, ab); };
   for (int i = next(); i >= 0 && ok; i = next()) {
     const Tile t = load_tile(a.tiles, i);
     if (t.cost == 0) continue;
     const int kv0 = a.pb.kv_off[t.b];
-    const int qrow = (a.pb.q_off ? a.pb.q_off[t.b] : 0) + (kPack ? max(t.blk, 0) : t.blk) * 128;
+    const int mblk = kPair ? 2 * t.blk + int(rank) : (kPack ? max(t.blk, 0) : t.blk);
+    const int qrow = (a.pb.q_off ? a.pb.q_off[t.b] : 0) + mblk * 128;
     const int x0 = t.h * D;
     ok = mbar_wait(smem_u32(&bars.q_empty), (nq & 1) ^ 1, ab);
     if (!ok) break;
@@ -138,22 +190,28 @@ __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const C
     auto load_k = [&](int j) -> bool {
       const uint32_t st = nk % C::kStages, ph = (nk / C::kStages) & 1;
       if (!mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, ab)) return false;
-      mbar_arrive_expect_tx(smem_u32(&bars.k_full[st]), C::kTileBytes);
+      mbar_arrive_expect_tx(smem_u32(&bars.k_full[st]), C::kKBytes);
 #pragma unroll
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_2d(sbase + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes, k_map,
-                    smem_u32(&bars.k_full[st]), x0 + c * 64, kv0 + j * 128);
+      for (int c = 0; c < C::kChunks; ++c)  // a pair's CTA: its 64 of the block's keys
+        tma_load_2d(sbase + C::kOffK + st * C::kKBytes + c * C::kKChunkBytes, k_map,
+                    smem_u32(&bars.k_full[st]), x0 + c * 64, kv0 + j * 128 + (kPair ? 64 * int(rank) : 0));
       ++nk;
+      prefetch_to(nk + C::kPrefetch);
       return true;
     };
     auto load_v = [&](int j) -> bool {
       const uint32_t st = nv % C::kStages, ph = (nv / C::kStages) & 1;
       if (!mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, ab)) return false;
-      mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), C::kTileBytes);
+      mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), C::kVBytes);
+      if constexpr (kPair) {  // its 64 of the head's D columns, all 128 keys
+        tma_load_2d(sbase + C::kOffV + st * C::kVBytes, v_map, smem_u32(&bars.v_full[st]),
+                    x0 + 64 * int(rank), kv0 + j * 128);
+      } else {
 #pragma unroll
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_2d(sbase + C::kOffV + st * C::kTileBytes + c * C::kChunkBytes, v_map,
-                    smem_u32(&bars.v_full[st]), x0 + c * 64, kv0 + j * 128);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_2d(sbase + C::kOffV + st * C::kVBytes + c * C::kChunkBytes, v_map,
+                      smem_u32(&bars.v_full[st]), x0 + c * 64, kv0 + j * 128);
+      }
       ++nv;
       return true;
     };
@@ -180,31 +238,54 @@ __device__ void fwd_producer(const FwdArgs& a, const CUtensorMap* q_map, const C
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread)
+// MMA issuer (one thread).  kPair: the even CTA's thread issues the pair's
+// products -- S = Q K^T with M = 256 (each CTA's 128 query rows) and N = 128
+// keys (each CTA's 64-key half of K), and O += P V with P from each CTA's
+// TMEM and V's D columns split in halves -- and commits each to the barrier
+// of that name in both CTAs.  It waits for the odd CTA's loads through the
+// *_pair barriers (the odd CTA's forwarder arrives on them) and for the
+// softmax warps of both CTAs (s_empty, p_full, o_empty count one arrival per
+// warp of either CTA).
 // ---------------------------------------------------------------------------
-template <int D, class Seq>
+template <int D, bool kPair, class Seq>
 __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars& bars,
                         const Abort& ab, Seq& seq) {
-  using C = FwdCfg<D>;
-  constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-  constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+  using C = FwdCfg<D, kPair>;
+  constexpr int M = kPair ? 256 : 128;
+  constexpr uint32_t idesc_qk = idesc_bf16_f32(M, 128, false, false);
+  constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, false, true);
   const uint64_t qd = smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
   uint32_t g = 0, tq = 0;
+  // phases the other CTA's threads arrive on are acquired at cluster scope
+  auto wait_x = [&](uint32_t bar, uint32_t parity) -> bool {
+    if constexpr (kPair) return mbar_wait_cluster(bar, parity, ab);
+    else return mbar_wait(bar, parity, ab);
+  };
+  auto commit = [&](uint32_t bar) {
+    if constexpr (kPair) mma_commit_pair(bar);
+    else mma_commit(bar);
+  };
 
   // O += P_gp V_gp; `first` marks the first block of a tile (overwrite O).
   auto issue_pv = [&](uint32_t gp, bool first) -> bool {
-    const uint32_t pb = gp & 1, st = gp % C::kStages;
-    if (first && !mbar_wait(smem_u32(&bars.o_empty), (tq & 1) ^ 1, ab)) return false;
-    if (!mbar_wait(smem_u32(&bars.p_full[pb]), (gp >> 1) & 1, ab)) return false;
-    if (!mbar_wait(smem_u32(&bars.v_full[st]), (gp / C::kStages) & 1, ab)) return false;
+    const uint32_t pb = gp & 1, st = gp % C::kStages, ph = (gp / C::kStages) & 1;
+    if (first && !wait_x(smem_u32(&bars.o_empty), (tq & 1) ^ 1)) return false;
+    if (!wait_x(smem_u32(&bars.p_full[pb]), (gp >> 1) & 1)) return false;
+    if (!mbar_wait(smem_u32(&bars.v_full[st]), ph, ab)) return false;
+    if (kPair && !wait_x(smem_u32(&bars.v_pair[st]), ph)) return false;
     tc_fence_after();
-    const uint64_t vd = smem_desc_sw128(sbase + C::kOffV + st * C::kTileBytes, C::kChunkBytes, 1024);
+    const uint64_t vd = smem_desc_sw128(sbase + C::kOffV + st * C::kVBytes, C::kChunkBytes, 1024);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-      mma_bf16_ts(tmem + C::kColO, tmem + C::kColP + pb * 64 + kk * 8, desc_at(vd, kk * 2048), idesc_pv,
-                  (first && kk == 0) ? 0u : 1u);
-    mma_commit(smem_u32(&bars.v_empty[st]));
-    mma_commit(smem_u32(&bars.pv_done[pb]));
+    for (int kk = 0; kk < 8; ++kk) {
+      if constexpr (kPair)
+        mma_pair_ts(tmem + C::kColO, tmem + C::kColP + pb * 64 + kk * 8, desc_at(vd, kk * 2048), idesc_pv,
+                    (first && kk == 0) ? 0u : 1u);
+      else
+        mma_bf16_ts(tmem + C::kColO, tmem + C::kColP + pb * 64 + kk * 8, desc_at(vd, kk * 2048), idesc_pv,
+                    (first && kk == 0) ? 0u : 1u);
+    }
+    commit(smem_u32(&bars.v_empty[st]));
+    commit(smem_u32(&bars.pv_done[pb]));
     return true;
   };
 
@@ -214,22 +295,28 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
     const Tile t = load_tile(a.tiles, i);
     if (t.cost == 0) continue;
     ok = mbar_wait(smem_u32(&bars.q_full), tq & 1, ab);
+    if (kPair && ok) ok = wait_x(smem_u32(&bars.q_pair), tq & 1);
     for (int j = 0; j < t.cost && ok; ++j) {
-      const uint32_t gj = g + j, st = gj % C::kStages, sb = gj & 1;
-      ok = mbar_wait(smem_u32(&bars.k_full[st]), (gj / C::kStages) & 1, ab) &&
-           mbar_wait(smem_u32(&bars.s_empty[sb]), ((gj >> 1) & 1) ^ 1, ab);
+      const uint32_t gj = g + j, st = gj % C::kStages, sb = gj & 1, ph = (gj / C::kStages) & 1;
+      ok = mbar_wait(smem_u32(&bars.k_full[st]), ph, ab) &&
+           (!kPair || wait_x(smem_u32(&bars.k_pair[st]), ph)) &&
+           wait_x(smem_u32(&bars.s_empty[sb]), ((gj >> 1) & 1) ^ 1);
       if (!ok) break;
       tc_fence_after();
-      const uint64_t kd = smem_desc_sw128(sbase + C::kOffK + st * C::kTileBytes, 16, 1024);
+      const uint64_t kd = smem_desc_sw128(sbase + C::kOffK + st * C::kKBytes, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-        mma_bf16_ss(tmem + C::kColS + sb * 128, desc_at(qd, koff), desc_at(kd, koff), idesc_qk,
-                    kk > 0 ? 1u : 0u);
+        const uint32_t koff = (kk & 3) * 32;
+        if constexpr (kPair)
+          mma_pair_ss(tmem + C::kColS + sb * 128, desc_at(qd, (kk >> 2) * C::kChunkBytes + koff),
+                      desc_at(kd, (kk >> 2) * C::kKChunkBytes + koff), idesc_qk, kk > 0 ? 1u : 0u);
+        else
+          mma_bf16_ss(tmem + C::kColS + sb * 128, desc_at(qd, (kk >> 2) * C::kChunkBytes + koff),
+                      desc_at(kd, (kk >> 2) * C::kKChunkBytes + koff), idesc_qk, kk > 0 ? 1u : 0u);
       }
-      mma_commit(smem_u32(&bars.s_full[sb]));
-      mma_commit(smem_u32(&bars.k_empty[st]));
-      if (j == t.cost - 1) mma_commit(smem_u32(&bars.q_empty));
+      commit(smem_u32(&bars.s_full[sb]));
+      commit(smem_u32(&bars.k_empty[st]));
+      if (j == t.cost - 1) commit(smem_u32(&bars.q_empty));
       if (j >= 1) ok = issue_pv(gj - 1, j == 1);
     }
     if (ok) ok = issue_pv(g + t.cost - 1, t.cost == 1);
@@ -237,17 +324,45 @@ __device__ void fwd_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, FwdBars
     ++tq;
   }
   // every MMA issued above has completed once this commit arrives
-  mma_commit(smem_u32(&bars.drain));
+  commit(smem_u32(&bars.drain));
   drain_wait(smem_u32(&bars.drain), 0);
+}
+
+// The odd CTA of a pair: after each of its own loads lands, tell the even
+// CTA's MMA issuer (which cannot wait on another CTA's barrier) through the
+// matching *_pair barrier there.  One thread, walking the same loads as the
+// producer.
+template <int D, class Seq>
+__device__ void fwd_pair_forwarder(const FwdArgs& a, FwdBars& bars, const Abort& ab, Seq& seq) {
+  using C = FwdCfg<D, true>;
+  uint32_t nq = 0, nk = 0, nv = 0;
+  auto next = [&] { return seq.take(a.dyn_counter, bars.ring, ab); };
+  for (int i = next(); i >= 0; i = next()) {
+    const Tile t = load_tile(a.tiles, i);
+    if (t.cost == 0) continue;
+    if (!mbar_wait(smem_u32(&bars.q_full), nq & 1, ab)) return;
+    mbar_arrive_rank0(smem_u32(&bars.q_pair));
+    ++nq;
+    for (int j = 0; j < t.cost; ++j) {
+      uint32_t st = nk % C::kStages;
+      if (!mbar_wait(smem_u32(&bars.k_full[st]), (nk / C::kStages) & 1, ab)) return;
+      mbar_arrive_rank0(smem_u32(&bars.k_pair[st]));
+      ++nk;
+      st = nv % C::kStages;
+      if (!mbar_wait(smem_u32(&bars.v_full[st]), (nv / C::kStages) & 1, ab)) return;
+      mbar_arrive_rank0(smem_u32(&bars.v_pair[st]));
+      ++nv;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
 // softmax / correction / epilogue (warps 0-3, thread = query row = TMEM lane)
 // ---------------------------------------------------------------------------
-template <int D, bool kPack, class Seq>
+template <int D, bool kPack, bool kPair, class Seq>
 __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t* smem, uint32_t tmem,
-                            FwdBars& bars, const Abort& ab, Seq& seq, int grp) {
-  using C = FwdCfg<D>;
+                            FwdBars& bars, const Abort& ab, Seq& seq, int grp, uint32_t rank) {
+  using C = FwdCfg<D, kPair>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;  // row of the tile, TMEM lane
   const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -258,6 +373,21 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
   const float sl2 = a.scale_log2;
   const int H = a.pb.H;
   uint32_t g = 0, tq = 0;
+  // an arrival the MMA issuer waits for: each thread's, or (CTA pairs) one per
+  // warp, on the barrier in the even CTA, whose thread issues for both.  These
+  // report tensor-memory reads and stores the warp has waited for, so the odd
+  // CTA's remote arrival needs no release of its other memory writes.
+  auto arrive_mma = [&](uint32_t bar) {
+    if constexpr (kPair) {
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(bar);
+        else mbar_arrive_rank0_relaxed(bar);
+      }
+    } else {
+      mbar_arrive(bar);
+    }
+  };
 
   auto next = [&] { return seq.take_warp(a.dyn_counter, bars.ring, ab); };
   for (int i = next(); i >= 0; i = next()) {
@@ -265,7 +395,7 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
     // packed tile (blk = -nseq): rows [off[b], off[b + nseq]) of nseq short
     // sequences, one key block, each row masked to its own sequence's keys
     const bool packed = kPack && t.blk < 0;
-    const int mblk = packed ? 0 : t.blk;
+    const int mblk = kPair ? 2 * t.blk + int(rank) : packed ? 0 : t.blk;
     const int64_t qlen = a.pb.q_off ? (a.pb.q_off[t.b + (packed ? -t.blk : 1)] - a.pb.q_off[t.b]) : a.pb.Lq;
     const int64_t o_first = (a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq) + mblk * 128;
     const bool row_ok = int64_t(mblk) * 128 + r < qlen;
@@ -312,7 +442,7 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
           for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(vv[c][e]);
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.s_empty[sb]));
+      arrive_mma(smem_u32(&bars.s_empty[sb]));
       if (j == t.cost - 1) {  // peeled tail: keys outside the sequence
         if (packed) {
 #pragma unroll
@@ -384,7 +514,7 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
       tc_fence_before();
       // (failure-path test: CTA 0's first warp withholds its first arrival)
       if (!(a.test_skip == 1 && blockIdx.x == 0 && warp == 0 && gj == 0))
-        mbar_arrive(smem_u32(&bars.p_full[sb]));
+        arrive_mma(smem_u32(&bars.p_full[sb]));
       m_run = m_new;
     }
     // epilogue: combine the groups' row sums, wait for the last PV,
@@ -418,7 +548,7 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
       tmem_ld_x32(tl + C::kColO + o0, ov[0]);
     }
     tc_fence_before();
-    mbar_arrive(smem_u32(&bars.o_empty));  // O's columns are free for the next tile
+    arrive_mma(smem_u32(&bars.o_empty));  // O's columns are free for the next tile
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
       const uint32_t (&v)[32] = ov[c];
@@ -451,92 +581,132 @@ __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t*
   }
 }
 
-template <int D, bool kPack, bool kDyn>
-__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+template <int D, bool kPack, bool kDyn, bool kPair>
+__global__ void __launch_bounds__(FwdCfg<D, kPair>::kThreads, 1)
     jfa_fwd_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map,
                    const __grid_constant__ CUtensorMap o_map, const FwdArgs a) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   FwdBars& bars = *reinterpret_cast<FwdBars*>(smem + C::kOffBar);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = kPair ? cluster_rank() : 0;
+  // arrivals the MMA issuer waits for: every softmax thread, or one per softmax
+  // warp of both CTAs of a pair
+  constexpr uint32_t kSoftmaxArrivals = kPair ? 16 : 256;
   if (tid == 0) {
     tile_ring_init(bars.ring, 1 + 8);  // consumers: the MMA thread and the 8 softmax warps
     mbar_init(smem_u32(&bars.q_full), 1);
     mbar_init(smem_u32(&bars.q_empty), 1);
+    mbar_init(smem_u32(&bars.q_pair), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
       mbar_init(smem_u32(&bars.k_empty[s]), 1);
       mbar_init(smem_u32(&bars.v_full[s]), 1);
       mbar_init(smem_u32(&bars.v_empty[s]), 1);
+      mbar_init(smem_u32(&bars.k_pair[s]), 1);
+      mbar_init(smem_u32(&bars.v_pair[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.s_full[s]), 1);
-      mbar_init(smem_u32(&bars.s_empty[s]), 256);
-      mbar_init(smem_u32(&bars.p_full[s]), 256);
+      mbar_init(smem_u32(&bars.s_empty[s]), kSoftmaxArrivals);
+      mbar_init(smem_u32(&bars.p_full[s]), kSoftmaxArrivals);
       for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bars.max_ready[s][q]), 64);
       for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bars.sum_ready[s][q]), 64);
       mbar_init(smem_u32(&bars.pv_done[s]), 1);
     }
-    mbar_init(smem_u32(&bars.o_empty), 256);
+    mbar_init(smem_u32(&bars.o_empty), kSoftmaxArrivals);
     mbar_init(smem_u32(&bars.drain), 1);
     bars.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == C::kMmaWarp) {
-    tmem_alloc(smem_u32(&bars.tmem_base), C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(&bars.tmem_base), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&bars.tmem_base), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   const Abort ab{&bars.abort_flag, a.status, a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs};
-  TileSeq<kDyn> seq(a.cta_ptr, a.dyn_counter);
+  // a pair's two CTAs walk the pair's slice of the schedule
+  TileSeq<kDyn> seq(a.cta_ptr, a.dyn_counter, kPair ? int(blockIdx.x >> 1) : int(blockIdx.x));
 
   if (warp == C::kProducerWarp) {
-    if (lane == 0) fwd_producer<D, kPack>(a, &q_map, &k_map, &v_map, sbase, bars, ab, seq);
+    if (lane == 0) fwd_producer<D, kPack, kPair>(a, &q_map, &k_map, &v_map, sbase, bars, ab, seq, rank);
     __syncwarp();
   } else if (warp == C::kMmaWarp) {
-    if (lane == 0) fwd_mma<D>(a, sbase, tmem, bars, ab, seq);
+    if (lane == 0) {
+      if (rank == 0) {
+        fwd_mma<D, kPair>(a, sbase, tmem, bars, ab, seq);
+      } else if constexpr (kPair) {
+        fwd_pair_forwarder<D>(a, bars, ab, seq);
+        drain_wait(smem_u32(&bars.drain), 0);  // the even CTA's last products have completed
+      }
+    }
     __syncwarp();
   } else {
-    fwd_softmax<D, kPack>(a, &o_map, smem, tmem, bars, ab, seq, warp >> 2);
+    fwd_softmax<D, kPack, kPair>(a, &o_map, smem, tmem, bars, ab, seq, warp >> 2, rank);
     if (lane == 0) bulk_wait_all();  // O boxes written before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // neither CTA leaves while the pair's products run
   if (warp == C::kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem, C::kTmemCols);
+    else tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-template <int D, bool kPack, bool kDyn>
+template <int D, bool kPack, bool kDyn, bool kPair>
 cudaError_t launch_fwd_d(const FwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, const CUtensorMap& o, int grid, cudaStream_t stream) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, kPair>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   static_assert(sizeof(FwdBars) <= C::kBarBytes, "barrier block");
-  cudaError_t e = set_smem_limit_once<jfa_fwd_kernel<D, kPack, kDyn>>(C::kSmemBytes);
+  cudaError_t e = set_smem_limit_once<jfa_fwd_kernel<D, kPack, kDyn, kPair>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  jfa_fwd_kernel<D, kPack, kDyn><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, o, a);
+  if constexpr (kPair) {  // clusters of two CTAs, grid = 2 x pairs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, jfa_fwd_kernel<D, kPack, kDyn, kPair>, q, k, v, o, a);
+    if (e != cudaSuccess) return e;
+  } else {
+    jfa_fwd_kernel<D, kPack, kDyn, kPair><<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, o, a);
+  }
   return cudaGetLastError();
 }
 
-// packed plans and dynamic schedules run their own instantiations
+// packed plans, dynamic schedules and CTA pairs run their own instantiations
 template <int D>
 cudaError_t launch_fwd_m(const FwdArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, const CUtensorMap& o, int grid, cudaStream_t stream) {
   if (a.dyn_counter)
-    return a.packed ? launch_fwd_d<D, true, true>(a, q, k, v, o, grid, stream)
-                    : launch_fwd_d<D, false, true>(a, q, k, v, o, grid, stream);
-  return a.packed ? launch_fwd_d<D, true, false>(a, q, k, v, o, grid, stream)
-                  : launch_fwd_d<D, false, false>(a, q, k, v, o, grid, stream);
+    return a.packed ? launch_fwd_d<D, true, true, false>(a, q, k, v, o, grid, stream)
+                    : launch_fwd_d<D, false, true, false>(a, q, k, v, o, grid, stream);
+  return a.packed ? launch_fwd_d<D, true, false, false>(a, q, k, v, o, grid, stream)
+                  : launch_fwd_d<D, false, false, false>(a, q, k, v, o, grid, stream);
 }
 
 }  // namespace
@@ -547,6 +717,10 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtenso
   if (grid <= 0) return cudaSuccess;
   // plans with packed short sequences run an instantiation that handles
   // packed tiles; the others keep the plain code path
+  if (a.pair) {  // D = 128, static schedule, plain tiles: grid = 2 x pairs
+    if (a.pb.D != 128 || a.packed || a.dyn_counter || (grid & 1)) return cudaErrorInvalidValue;
+    return launch_fwd_d<128, false, false, true>(a, q_map, k_map, v_map, o_map, grid, stream);
+  }
   if (a.pb.D == 128)
     return launch_fwd_m<128>(a, q_map, k_map, v_map, o_map, grid, stream);
   return launch_fwd_m<64>(a, q_map, k_map, v_map, o_map, grid, stream);

@@ -47,6 +47,9 @@ struct FwdArgs {
   // (0: the default) and, with test_skip = 1, one arrival withheld
   uint64_t wait_limit_ns = 0;
   int test_skip = 0;
+  // CTA pairs (D = 128, static, no packing): the schedule lists pair tiles
+  // {b, h, mp, cost} -- query blocks 2 mp and 2 mp + 1 -- over grid / 2 slots
+  bool pair = false;
 };
 
 struct BwdArgs {

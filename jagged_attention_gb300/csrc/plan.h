@@ -62,6 +62,9 @@ struct jfa_plan {
   // tile meets all the keys of its queries and forms Delta itself: the
   // pre-pass skips the Delta kernel (unless JFA_PLAN_DELTA_PREPASS)
   bool own_delta = false;
+  // the forward runs as CTA pairs over pairs of query blocks; `fwd` then
+  // holds the pair schedule, P pairs (2 P CTAs)
+  bool fwd_pair = false;
   // failure-path test only (jfa_plan_selftest)
   int test_skip = 0;
   uint64_t test_limit_ns = 0;

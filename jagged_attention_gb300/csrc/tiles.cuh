@@ -38,6 +38,9 @@ struct TileSeq<false> {
   int i, end;
   __device__ TileSeq(const int32_t* cta_ptr, const int*)
       : i(cta_ptr[blockIdx.x]), end(cta_ptr[blockIdx.x + 1]) {}
+  // slot: the schedule's CTA index (a pair of CTAs shares one)
+  __device__ TileSeq(const int32_t* cta_ptr, const int*, int slot)
+      : i(cta_ptr[slot]), end(cta_ptr[slot + 1]) {}
   __device__ int claim(int*, int, TileRing&, const Abort&) { return i < end ? i++ : -1; }
   __device__ int take(const int*, TileRing&, const Abort&) { return i < end ? i++ : -1; }
   __device__ int take_warp(const int*, TileRing&, const Abort&) { return i < end ? i++ : -1; }
@@ -47,6 +50,7 @@ template <>
 struct TileSeq<true> {
   uint32_t k;  // ring entries handled
   __device__ TileSeq(const int32_t*, const int*) : k(0) {}
+  __device__ TileSeq(const int32_t*, const int*, int) : k(0) {}
 
   // The claiming thread: claims the next tile and publishes it to the ring.
   __device__ int claim(int* counter, int T, TileRing& ring, const Abort& ab) {

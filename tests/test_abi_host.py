@@ -31,7 +31,7 @@ def test_binding_constants_match_the_header():
     flags = {m[0]: int(m[1]) for m in re.findall(r"#define JFA_PLAN_(\w+) (\d+)u", text)}
     assert flags == {"PACK_SHORT": jfa.PLAN_PACK_SHORT, "DYNAMIC": jfa.PLAN_DYNAMIC,
                      "DELTA_PREPASS": jfa.PLAN_DELTA_PREPASS, "DELTA_IN_TILES": jfa.PLAN_DELTA_IN_TILES,
-                     "NO_PACK": jfa.PLAN_NO_PACK}
+                     "NO_PACK": jfa.PLAN_NO_PACK, "FWD_PAIRS": jfa.PLAN_FWD_PAIRS}
     codes = {int(m[1]): m[0] for m in re.findall(r"\b(JFA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text)}
     assert codes == jfa.STATUS_NAMES
 
@@ -110,6 +110,38 @@ def test_native_builder_matches_reference_on_workloads(name):
         assert np.array_equal(t, rt) and np.array_equal(p, rp)
 
 
+@pytest.mark.parametrize("name", sorted(workloads.WORKLOADS))
+def test_pair_schedule_matches_reference_on_workloads(name):
+    # the forward over pair tiles (two query blocks per tile, the CTA-pair
+    # kernel) is the forward schedule of the half-length query sequences
+    w = workloads.WORKLOADS[name]
+    klen = workloads.draw_lengths(w.lengths, w.B, 0)
+    kv = workloads.offsets_from_lengths(klen)
+    if w.mode == "broadcast":
+        qlen, qo, Lq = np.full(w.B, w.Lq), None, w.Lq
+    else:
+        qlen, qo, Lq = klen, kv, 0
+    t, p = jfa.build_tiles(kv, qo, H=w.H, Lq=Lq, num_ctas=76, direction=2)
+    rt, rp = _ref((qlen + 1) // 2, klen, w.H, 76, 0)
+    assert np.array_equal(t, rt) and np.array_equal(p, rp)
+    # every query block of every (sequence, head) is in exactly one pair tile
+    nblk = (qlen + 127) // 128
+    assert t.shape[0] == w.H * int(((nblk + 1) // 2).sum())
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_pair_schedule_matches_reference_random(seed):
+    rng = np.random.default_rng(500 + seed)
+    B = int(rng.integers(1, 60))
+    klen = rng.integers(0, 900, size=B)
+    qlen = rng.integers(0, 900, size=B)
+    kv, qo = workloads.offsets_from_lengths(klen), workloads.offsets_from_lengths(qlen)
+    P = int(rng.integers(1, 80))
+    t, p = jfa.build_tiles(kv, qo, H=2, num_ctas=P, direction=2)
+    rt, rp = _ref((qlen + 1) // 2, klen, 2, P, 0)
+    assert np.array_equal(t, rt) and np.array_equal(p, rp)
+
+
 @pytest.mark.parametrize("seed", range(8))
 def test_native_packed_builder_matches_reference_random(seed):
     rng = np.random.default_rng(300 + seed)
@@ -182,8 +214,9 @@ def test_rejects_bad_arguments_before_touching_the_device():
     assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 0, 0, None, None,
                              ctypes.byref(T), ctypes.byref(P)) == 3
     kv = np.array([0, 4, 6], dtype=np.int32)
-    assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 2, 0, None, None,
-                             ctypes.byref(T), ctypes.byref(P)) == 1  # bad direction
+    assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 3, 0, None, None,
+                             ctypes.byref(T), ctypes.byref(P)) == 1  # bad direction (0, 1, 2 exist)
+    assert L.jfa_plan_forward_pairs(None, None) == 1
     assert L.jfa_fwd(None, None, None, None, 1.0, None, None, None) == 1
     assert L.jfa_bwd(None, None, None, None, None, None, None, 1.0, None, None, None, None, 0,
                      None) == 1

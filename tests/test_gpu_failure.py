@@ -44,17 +44,23 @@ def test_plan_selftest_rejects_bad_arguments():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("skip", [1, 2])
-def test_real_kernel_timeout_cascade(skip):
+@pytest.mark.parametrize("skip,flags", [(1, 0), (2, 0), (1, jfa.PLAN_FWD_PAIRS)])
+def test_real_kernel_timeout_cascade(skip, flags):
     """One softmax warp of CTA 0 withholds one arrival (skip 1: the forward's
     first P block, 2: the backward's first dS^T), with every wait limited to
     20 ms: the MMA issuer's wait runs out, the abort reaches every role of the
     CTA (producer drain, MMA drain commit, TMEM release), the launch ends, the
     plan's status word reports JFA_ERR_DEVICE_TIMEOUT, and a normal forward
-    and backward right after still match the oracle."""
+    and backward right after still match the oracle.  With CTA pairs the odd
+    CTA's roles run out on their own waits (its loads' forwarder, its softmax
+    warps) and both CTAs meet at the cluster barrier before releasing TMEM."""
     import torch
-    p = parity.to_cuda(workloads.make_workload("tiny_broadcast", seed=0))
-    plan = parity.make_plan(p)
+    if flags & jfa.PLAN_FWD_PAIRS:  # D = 128, two query blocks: a pair tile per sequence
+        p = parity.to_cuda(workloads.make_problem(3, 2, 128, "broadcast", [300, 5, 128], Lq=256, seed=57))
+    else:
+        p = parity.to_cuda(workloads.make_workload("tiny_broadcast", seed=0))
+    plan = parity.make_plan(p, 0, flags)
+    assert plan.forward_pairs() == bool(flags & jfa.PLAN_FWD_PAIRS)
     out, lse, _ = parity.gpu_fwd(p, plan)
     plan.selftest(skip, 20000)
     if skip == 1:
