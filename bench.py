@@ -45,8 +45,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # 256-sequence capture of the same kernel, scaled by K/V tokens: x3.730),
 # keyed by kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2559e+09, "src_hash": "bcfe3c17d7a8944e"},
-    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7861e+09, "src_hash": "90ee7b645f18074f"},
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2422e+09, "src_hash": "0c0612018e8548c4"},
+    "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7855e+09, "src_hash": "1563cbaeaea90a38"},
+    "jfa_fwd_kernel:gem_broadcast:pairs": {"bytes": 1.7879e+09, "src_hash": "1563cbaeaea90a38"},
 }
 
 
@@ -524,7 +525,8 @@ def run_ours(args, rank, world, dist):
     dom = per_kernel[dom_name]
     ridge = tf_peak * 1e12 / (bw_peak * 1e9)
     ai = dom["flops"] / dom["bytes"]
-    key = f"{dom_name}:{args.workload}"
+    # stored counters are per kernel form: the pair forward is its own kernel
+    key = f"{dom_name}:{args.workload}" + (":pairs" if dom_name == "jfa_fwd_kernel" and plan.forward_pairs() else "")
     tr = NCU_TRAFFIC.get(key)
     traffic = tr["bytes"] if tr and tr.get("src_hash") == src_hash(dom["src"]) else None
     if ai >= ridge:
@@ -565,7 +567,8 @@ def run_ours(args, rank, world, dist):
                    "parallelism": (f"dp{world} (one batch split by sequence, broadcast dQ all-reduced)"
                                    if split else f"dp{world} (independent batches)"),
                    "plan": ("short sequences packed" if pack else "plain schedule")
-                           + (", tiles claimed at run time" if args.dynamic else ""),
+                           + (", tiles claimed at run time" if args.dynamic else "")
+                           + (", forward as CTA pairs" if plan.forward_pairs() else ""),
                    "delta": "formed by the backward tiles" if own_delta else "pre-pass"},
         "fwd_tflops": per_kernel["jfa_fwd_kernel"]["tflops"],
         "bwd_tflops": flops(prob, "bwd") / ((k_pre + k_main) / args.steps * 1e-3) / 1e12,
@@ -593,7 +596,8 @@ def plan_flags(args, jfa) -> int:
     return ((jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_NO_PACK if args.no_pack else 0)
             | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
             | (jfa.PLAN_DELTA_PREPASS if args.delta_prepass else 0)
-            | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0))
+            | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0)
+            | (jfa.PLAN_FWD_PAIRS if args.fwd_pairs else 0))
 
 
 def run_e2e(args, prob, dev, stream, jfa):
@@ -692,6 +696,8 @@ def main():
                     help="pack short sequences into shared tiles wherever a run forms (by default "
                          "the library packs when that removes an eighth of the tiles)")
     pk.add_argument("--no-pack", action="store_true", help="never pack short sequences")
+    ap.add_argument("--fwd-pairs", action="store_true",
+                    help="run the forward as CTA pairs where the plan allows (JFA_PLAN_FWD_PAIRS)")
     ap.add_argument("--batch", type=int, default=None,
                     help="keep only the first B sequences of the workload (profiling captures)")
     ap.add_argument("--split-batch", action="store_true",
