@@ -567,7 +567,7 @@ def run_ours(args, rank, world, dist):
                    "parallelism": (f"dp{world} (one batch split by sequence, broadcast dQ all-reduced)"
                                    if split else f"dp{world} (independent batches)"),
                    "plan": ("short sequences packed" if pack else "plain schedule")
-                           + (", tiles claimed at run time" if args.dynamic else "")
+                           + claims_note(plan)
                            + (", forward as CTA pairs" if plan.forward_pairs() else ""),
                    "delta": "formed by the backward tiles" if own_delta else "pre-pass"},
         "fwd_tflops": per_kernel["jfa_fwd_kernel"]["tflops"],
@@ -592,9 +592,18 @@ def pack_mode(args) -> str:
     return "force" if args.pack else ("off" if args.no_pack else "auto")
 
 
+def claims_note(plan) -> str:
+    fwd, bwd = plan.claims()
+    if fwd and bwd:
+        return ", tiles claimed at run time"
+    if fwd or bwd:
+        return ", " + ("forward" if fwd else "backward") + " tiles claimed at run time"
+    return ""
+
+
 def plan_flags(args, jfa) -> int:
     return ((jfa.PLAN_PACK_SHORT if args.pack else 0) | (jfa.PLAN_NO_PACK if args.no_pack else 0)
-            | (jfa.PLAN_DYNAMIC if args.dynamic else 0)
+            | (jfa.PLAN_DYNAMIC if args.dynamic else 0) | (jfa.PLAN_STATIC if args.static else 0)
             | (jfa.PLAN_DELTA_PREPASS if args.delta_prepass else 0)
             | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0)
             | (jfa.PLAN_FWD_PAIRS if args.fwd_pairs else 0))
@@ -685,8 +694,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--dynamic", action="store_true",
-                    help="claim tiles at run time (JFA_PLAN_DYNAMIC) instead of the host deal")
+    sc = ap.add_mutually_exclusive_group()
+    sc.add_argument("--dynamic", action="store_true",
+                    help="claim both passes' tiles at run time (JFA_PLAN_DYNAMIC; by default the "
+                         "library claims the backward's in self mode only)")
+    sc.add_argument("--static", action="store_true",
+                    help="deal both passes' tiles on the host (JFA_PLAN_STATIC)")
     ap.add_argument("--delta-prepass", action="store_true",
                     help="form Delta in the pre-pass even where the backward tiles could (A/B)")
     ap.add_argument("--delta-in-tiles", action="store_true",

@@ -119,8 +119,15 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
  * counter lives in the plan and is reset on the stream before each launch,
  * so a plan's launches must be stream-ordered.  Combines with
  * JFA_PLAN_PACK_SHORT.
+ * JFA_PLAN_DYNAMIC claims the tiles of both passes; JFA_PLAN_STATIC deals
+ * both on the host (the two together are invalid).  Without either, the
+ * forward is dealt on the host, and the backward is claimed at run time when
+ * queries have their own offsets (self mode, where a sequence's key blocks
+ * make tiles of very different lengths) and dealt in broadcast mode, where
+ * claiming measured slower; jfa_plan_claims reports the choice.
  */
 #define JFA_PLAN_DYNAMIC 2u
+#define JFA_PLAN_STATIC 128u
 
 /*
  * Where Delta comes from.  When every sequence that has queries has at most
@@ -178,6 +185,11 @@ int jfa_plan_destroy(jfa_plan_t plan);
  */
 int jfa_plan_tiles(jfa_plan_t plan, int dir, int32_t* tiles_host, int32_t* cta_ptr_host, int* T,
                    int* P);
+
+/* *fwd / *bwd = 1 when that pass's tiles are claimed at run time (JFA_PLAN_DYNAMIC
+ * and the default rule given with it), 0 when they are dealt on the host.
+ * Either pointer may be NULL. */
+int jfa_plan_claims(jfa_plan_t plan, int* fwd, int* bwd);
 
 /* *pairs = 1 when the plan's forward runs as CTA pairs (JFA_PLAN_FWD_PAIRS), else 0. */
 int jfa_plan_forward_pairs(jfa_plan_t plan, int* pairs);

@@ -34,6 +34,7 @@ PLAN_DELTA_PREPASS = 4  # JFA_PLAN_DELTA_PREPASS
 PLAN_DELTA_IN_TILES = 8  # JFA_PLAN_DELTA_IN_TILES
 PLAN_NO_PACK = 32  # JFA_PLAN_NO_PACK
 PLAN_FWD_PAIRS = 64  # JFA_PLAN_FWD_PAIRS
+PLAN_STATIC = 128  # JFA_PLAN_STATIC
 
 
 class JfaError(RuntimeError):
@@ -92,13 +93,14 @@ def lib() -> ctypes.CDLL:
             L.jfa_plan_device_status.argtypes = [_vp, _vp, _ip]
             L.jfa_plan_selftest.argtypes = [_vp, ctypes.c_int, ctypes.c_uint]
             L.jfa_plan_forward_pairs.argtypes = [_vp, _ip]
+            L.jfa_plan_claims.argtypes = [_vp, _ip, _ip]
             L.jfa_status_string.argtypes = [ctypes.c_int]
             L.jfa_status_string.restype = ctypes.c_char_p
             for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
                          "jfa_fwd", "jfa_bwd", "jfa_bwd_preprocess", "jfa_bwd_main",
                          "jfa_plan_device_status", "jfa_delta_in_tiles", "jfa_fwd_simple",
                          "jfa_bwd_simple", "jfa_simple_device_status", "jfa_simple_release",
-                         "jfa_plan_selftest", "jfa_plan_forward_pairs"):
+                         "jfa_plan_selftest", "jfa_plan_forward_pairs", "jfa_plan_claims"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -210,6 +212,12 @@ class Plan:
                                 ptr.ctypes.data_as(_i32p), ctypes.byref(T), ctypes.byref(P)),
                "jfa_plan_tiles")
         return tiles, ptr
+
+    def claims(self) -> tuple:
+        """(forward, backward): whether each pass claims its tiles at run time."""
+        f, b = ctypes.c_int(), ctypes.c_int()
+        _check(lib().jfa_plan_claims(self.handle, ctypes.byref(f), ctypes.byref(b)), "jfa_plan_claims")
+        return bool(f.value), bool(b.value)
 
     def forward_pairs(self) -> bool:
         """Whether the plan's forward runs as CTA pairs over pair tiles."""

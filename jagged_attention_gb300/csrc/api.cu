@@ -171,6 +171,17 @@ std::vector<int64_t> pair_lengths(const std::vector<int64_t>& qlen) {
   return h;
 }
 
+// Which passes claim their tiles at run time: both with JFA_PLAN_DYNAMIC,
+// neither with JFA_PLAN_STATIC, else the backward in self mode only.
+bool claims_fwd(unsigned flags) { return (flags & JFA_PLAN_DYNAMIC) != 0; }
+bool claims_bwd(unsigned flags, bool broadcast) {
+  return (flags & JFA_PLAN_DYNAMIC) != 0 || (!(flags & JFA_PLAN_STATIC) && !broadcast);
+}
+bool bad_flags(unsigned flags) {
+  return ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) ||
+         ((flags & JFA_PLAN_DYNAMIC) && (flags & JFA_PLAN_STATIC));
+}
+
 bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B,
                  const std::vector<int64_t>& kvlen, std::vector<int>* pack) {
   if ((flags & JFA_PLAN_NO_PACK) || !q_off) return false;
@@ -213,17 +224,17 @@ int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
                     int32_t* cta_ptr_out, int* T, int* P) {
   if (!kv_offsets_host || B < 1 || H < 1 || num_ctas < 1 || dir < 0 || dir > 2 || !T || !P)
     return JFA_ERR_INVALID_ARG;
-  if ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) return JFA_ERR_INVALID_ARG;
+  if (bad_flags(flags)) return JFA_ERR_INVALID_ARG;
   std::vector<int64_t> qlen, kvlen;
   int64_t n_kv = 0, n_q = 0;
   int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
   if (rc != JFA_OK) return rc;
   std::vector<int> pack;
   const bool packing = use_packing(flags, kv_offsets_host, q_offsets_host, B, kvlen, &pack);
-  const bool dyn = (flags & JFA_PLAN_DYNAMIC) != 0;
   const Schedule s =
-      dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, dyn)
-      : dir == 1 ? jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, dyn)
+      dir == 0 ? jfa::build_fwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr, claims_fwd(flags))
+      : dir == 1 ? jfa::build_bwd_schedule(qlen, kvlen, H, num_ctas, packing ? &pack : nullptr,
+                                          claims_bwd(flags, q_offsets_host == nullptr))
                  : jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, num_ctas, nullptr, false);
   *T = s.T;
   *P = s.P;
@@ -236,7 +247,7 @@ int jfa_delta_in_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_
                        int Lq, unsigned flags, int* in_tiles) {
   if (!kv_offsets_host || B < 1 || !in_tiles) return JFA_ERR_INVALID_ARG;
   if ((flags & JFA_PLAN_DELTA_PREPASS) && (flags & JFA_PLAN_DELTA_IN_TILES)) return JFA_ERR_INVALID_ARG;
-  if ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) return JFA_ERR_INVALID_ARG;
+  if (bad_flags(flags)) return JFA_ERR_INVALID_ARG;
   std::vector<int64_t> qlen, kvlen;
   int64_t n_kv = 0, n_q = 0;
   int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
@@ -259,7 +270,7 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   if (!out || !kv_offsets_host || B < 1 || H < 1 || num_ctas < 0) return JFA_ERR_INVALID_ARG;
   *out = nullptr;
   if ((flags & JFA_PLAN_DELTA_PREPASS) && (flags & JFA_PLAN_DELTA_IN_TILES)) return JFA_ERR_INVALID_ARG;
-  if ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) return JFA_ERR_INVALID_ARG;
+  if (bad_flags(flags)) return JFA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
   std::vector<int64_t> qlen, kvlen;
   int64_t n_kv = 0, n_q = 0;
@@ -314,12 +325,13 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
       p->dq_own_rows = true;
     }
   }
-  p->dynamic = (flags & JFA_PLAN_DYNAMIC) != 0;
-  p->fwd_pair = use_fwd_pairs(flags, D, p->packed, p->dynamic, p->num_ctas, qlen);
+  p->fwd_dynamic = claims_fwd(flags);
+  p->bwd_dynamic = claims_bwd(flags, p->broadcast);
+  p->fwd_pair = use_fwd_pairs(flags, D, p->packed, p->fwd_dynamic, p->num_ctas, qlen);
   p->fwd = p->fwd_pair ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas / 2, nullptr, false)
                        : jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr,
-                                                 p->dynamic);
-  p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->dynamic);
+                                                 p->fwd_dynamic);
+  p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->bwd_dynamic);
   p->own_delta = tiles_form_delta(flags, qlen, kvlen, p->bwd, kv_offsets_host);
   for (int b = 0; b < B; ++b) {
     if (qlen[b] == 0 && kvlen[b] > 0) {
@@ -379,6 +391,13 @@ int jfa_plan_destroy(jfa_plan_t plan) {
   if (plan->dev_block && cudaFree(plan->dev_block) != cudaSuccess) rc = JFA_ERR_CUDA;
   delete plan;
   return rc;
+}
+
+int jfa_plan_claims(jfa_plan_t plan, int* fwd, int* bwd) {
+  if (!plan) return JFA_ERR_INVALID_ARG;
+  if (fwd) *fwd = plan->fwd_dynamic ? 1 : 0;
+  if (bwd) *bwd = plan->bwd_dynamic ? 1 : 0;
+  return JFA_OK;
 }
 
 int jfa_plan_forward_pairs(jfa_plan_t plan, int* pairs) {
@@ -446,7 +465,7 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
   a.T = plan->fwd.T;
   a.wait_limit_ns = plan->test_limit_ns;
   a.test_skip = plan->test_skip == 1 ? 1 : 0;
-  if (plan->dynamic) {
+  if (plan->fwd_dynamic) {
     a.dyn_counter = plan->d_counters;
     if (cudaMemsetAsync(a.dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return JFA_ERR_CUDA;
@@ -536,7 +555,7 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
   a.T = plan->bwd.T;
   a.wait_limit_ns = plan->test_limit_ns;
   a.test_skip = plan->test_skip == 2 ? 2 : 0;
-  if (plan->dynamic) {
+  if (plan->bwd_dynamic) {
     a.dyn_counter = plan->d_counters + 1;
     if (cudaMemsetAsync(a.dyn_counter, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return JFA_ERR_CUDA;

@@ -57,7 +57,8 @@ struct jfa_plan {
   // stores its rows)
   std::vector<std::pair<int64_t, int64_t>> dq_rows_to_clear;
   bool dq_own_rows = false;  // some rows are left to the tiles that own them
-  bool dynamic = false;      // tiles claimed at run time (JFA_PLAN_DYNAMIC)
+  bool fwd_dynamic = false;  // forward tiles claimed at run time
+  bool bwd_dynamic = false;  // backward tiles claimed at run time
   // every sequence with queries has at most one key block, so each backward
   // tile meets all the keys of its queries and forms Delta itself: the
   // pre-pass skips the Delta kernel (unless JFA_PLAN_DELTA_PREPASS)

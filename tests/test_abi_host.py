@@ -31,7 +31,8 @@ def test_binding_constants_match_the_header():
     flags = {m[0]: int(m[1]) for m in re.findall(r"#define JFA_PLAN_(\w+) (\d+)u", text)}
     assert flags == {"PACK_SHORT": jfa.PLAN_PACK_SHORT, "DYNAMIC": jfa.PLAN_DYNAMIC,
                      "DELTA_PREPASS": jfa.PLAN_DELTA_PREPASS, "DELTA_IN_TILES": jfa.PLAN_DELTA_IN_TILES,
-                     "NO_PACK": jfa.PLAN_NO_PACK, "FWD_PAIRS": jfa.PLAN_FWD_PAIRS}
+                     "NO_PACK": jfa.PLAN_NO_PACK, "FWD_PAIRS": jfa.PLAN_FWD_PAIRS,
+                     "STATIC": jfa.PLAN_STATIC}
     codes = {int(m[1]): m[0] for m in re.findall(r"\b(JFA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text)}
     assert codes == jfa.STATUS_NAMES
 
@@ -48,9 +49,13 @@ def test_native_builder_matches_hand_worked(case):
     bcast = len(set(ql.tolist())) == 1 and case["name"].startswith("broadcast")
     qo = None if bcast else workloads.offsets_from_lengths(ql)
     Lq = int(ql[0]) if bcast else 0
+    # the hand-worked lists are host deals unless the case claims tiles
+    flags = case.get("flags", 0)
+    if not flags & jfa.PLAN_DYNAMIC:
+        flags |= jfa.PLAN_STATIC
     for d, key in ((0, "fwd"), (1, "bwd")):
         t, p = jfa.build_tiles(kv, qo, H=case["H"], Lq=Lq, num_ctas=case["num_ctas"], direction=d,
-                               flags=case.get("flags", 0))
+                               flags=flags)
         assert np.array_equal(t, case[key]) and np.array_equal(p, case[f"{key}_cta_ptr"])
 
 
@@ -70,8 +75,12 @@ def test_native_builder_matches_reference_random(seed):
         qlen = rng.integers(0, 700, size=B)
         Lq, qo = 0, workloads.offsets_from_lengths(qlen)
     for d in (0, 1):
-        t, p = jfa.build_tiles(kv, qo, H=H, Lq=Lq, num_ctas=P, direction=d)
+        t, p = jfa.build_tiles(kv, qo, H=H, Lq=Lq, num_ctas=P, direction=d, flags=jfa.PLAN_STATIC)
         rt, rp = _ref(qlen, klen, H, P, d)
+        assert np.array_equal(t, rt) and np.array_equal(p, rp)
+        # by default the backward claims its tiles in self mode
+        t, p = jfa.build_tiles(kv, qo, H=H, Lq=Lq, num_ctas=P, direction=d)
+        rt, rp = _ref(qlen, klen, H, P, d, dynamic=(d == 1 and qo is not None))
         assert np.array_equal(t, rt) and np.array_equal(p, rp)
         t, p = jfa.build_tiles(kv, qo, H=H, Lq=Lq, num_ctas=P, direction=d, flags=jfa.PLAN_DYNAMIC)
         rt, rp = _ref(qlen, klen, H, P, d, dynamic=True)
@@ -100,13 +109,15 @@ def test_native_builder_matches_reference_on_workloads(name):
     else:
         qlen, qo, Lq = klen, kv, 0
     for d in (0, 1):
-        t, p = jfa.build_tiles(kv, qo, H=w.H, Lq=Lq, num_ctas=152, direction=d, flags=jfa.PLAN_NO_PACK)
+        t, p = jfa.build_tiles(kv, qo, H=w.H, Lq=Lq, num_ctas=152, direction=d,
+                               flags=jfa.PLAN_NO_PACK | jfa.PLAN_STATIC)
         rt, rp = _ref(qlen, klen, w.H, 152, d)
         assert np.array_equal(t, rt) and np.array_equal(p, rp)
-        # the default plan: packed where the default rule says so
+        # the default plan: packed where the default rule says so, the
+        # backward's tiles claimed at run time in self mode
         t, p = jfa.build_tiles(kv, qo, H=w.H, Lq=Lq, num_ctas=152, direction=d)
         pack = ref_tiles.short_packs(klen) if qo is not None and _auto_packs(klen) else None
-        rt, rp = _ref(qlen, klen, w.H, 152, d, pack)
+        rt, rp = _ref(qlen, klen, w.H, 152, d, pack, dynamic=(d == 1 and qo is not None))
         assert np.array_equal(t, rt) and np.array_equal(p, rp)
 
 
@@ -154,8 +165,11 @@ def test_native_packed_builder_matches_reference_random(seed):
     P = int(rng.integers(1, 100))
     pack = ref_tiles.short_packs(lens)
     for d in (0, 1):
-        t, p = jfa.build_tiles(kv, kv, H=H, num_ctas=P, direction=d, flags=jfa.PLAN_PACK_SHORT)
+        t, p = jfa.build_tiles(kv, kv, H=H, num_ctas=P, direction=d, flags=jfa.PLAN_PACK_SHORT | jfa.PLAN_STATIC)
         rt, rp = _ref(lens, lens, H, P, d, pack)
+        assert np.array_equal(t, rt) and np.array_equal(p, rp)
+        t, p = jfa.build_tiles(kv, kv, H=H, num_ctas=P, direction=d, flags=jfa.PLAN_PACK_SHORT)
+        rt, rp = _ref(lens, lens, H, P, d, pack, dynamic=(d == 1))
         assert np.array_equal(t, rt) and np.array_equal(p, rp)
     # different query offsets or broadcast mode: the flag is ignored
     t, _ = jfa.build_tiles(kv, kv.copy() + 0, H=H, num_ctas=P, direction=0, flags=jfa.PLAN_PACK_SHORT)
@@ -208,6 +222,8 @@ def test_rejects_bad_arguments_before_touching_the_device():
     assert _create(ok, None, 2, 1, -1, 128) == 1                     # negative Lq
     assert _create(ok, None, 2, 1, 4, 128,                           # Delta both ways
                    flags=jfa.PLAN_DELTA_PREPASS | jfa.PLAN_DELTA_IN_TILES) == 1
+    assert _create(ok, None, 2, 1, 4, 128,                           # claimed and dealt
+                   flags=jfa.PLAN_DYNAMIC | jfa.PLAN_STATIC) == 1
     L = jfa.lib()
     T, P = ctypes.c_int(), ctypes.c_int()
     kv = np.array([0, 4, 2], dtype=np.int32)
@@ -217,6 +233,9 @@ def test_rejects_bad_arguments_before_touching_the_device():
     assert L.jfa_build_tiles(kv.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 8, 3, 0, None, None,
                              ctypes.byref(T), ctypes.byref(P)) == 1  # bad direction (0, 1, 2 exist)
     assert L.jfa_plan_forward_pairs(None, None) == 1
+    assert L.jfa_plan_claims(None, None, None) == 1
+    with pytest.raises(jfa.JfaError):
+        jfa.build_tiles(kv, None, H=1, Lq=4, num_ctas=8, direction=1, flags=jfa.PLAN_DYNAMIC | jfa.PLAN_STATIC)
     assert L.jfa_fwd(None, None, None, None, 1.0, None, None, None) == 1
     assert L.jfa_bwd(None, None, None, None, None, None, None, 1.0, None, None, None, None, 0,
                      None) == 1

@@ -68,3 +68,19 @@ def test_repeated_launches_reset_the_counter():
     g1 = parity.gpu_bwd(p, o1, l1, plan)
     g2 = parity.gpu_bwd(p, o1, l1, plan)
     assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+
+
+def test_default_claims_rule():
+    # by default the backward claims its tiles in self mode and is dealt on
+    # the host in broadcast mode; the forward is dealt on the host; the flags
+    # force either way, and the default self-mode plan matches the oracle
+    self_p = parity.to_cuda(workloads.make_workload("jagged_self", seed=2))
+    bc = parity.to_cuda(workloads.make_workload("tiny_broadcast", seed=2))
+    assert parity.make_plan(self_p).claims() == (False, True)
+    assert parity.make_plan(bc).claims() == (False, False)
+    assert parity.make_plan(self_p, 0, jfa.PLAN_STATIC).claims() == (False, False)
+    assert parity.make_plan(bc, 0, DYN).claims() == (True, True)
+    plan = _run(workloads.make_workload("jagged_self", seed=2), 5, 0)
+    tiles, ptr = plan.tiles(1)
+    assert ptr[0] == 0 and (ptr[1:] == tiles.shape[0]).all()  # one claim queue
+    _run(workloads.make_workload("jagged_self", seed=2), 5, jfa.PLAN_STATIC)

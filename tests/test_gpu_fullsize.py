@@ -34,8 +34,9 @@ pytestmark = pytest.mark.gpu
 VARIANTS = {
     "gem_broadcast": [0, jfa.PLAN_DYNAMIC],
     "skewed_broadcast": [0],
-    # unpacked, packed by the default rule, packed with dynamic claiming
-    "block_diag": [jfa.PLAN_NO_PACK, 0, jfa.PLAN_DYNAMIC],
+    # unpacked, the default (packed, backward tiles claimed at run time), the
+    # same with both passes dealt on the host, both passes claimed
+    "block_diag": [jfa.PLAN_NO_PACK, 0, jfa.PLAN_STATIC, jfa.PLAN_DYNAMIC],
 }
 CHUNK_KV_ROWS = 1 << 17
 LOCAL_TOL = 2e-2
