@@ -344,6 +344,27 @@ int jfa_plan_selftest(jfa_plan_t plan, int skip, unsigned limit_us);
 int jfa_selftest_wait_timeout(unsigned limit_us, unsigned long long* waited_ns, void* stream);
 
 /*
+ * Diagnostic: what one tensor-core product costs on this GPU.  One CTA issues
+ * `count` (a multiple of 8, up to 2^20) tcgen05.mma products of one form back
+ * to back into one TMEM accumulator (bf16 operands, fp32 accumulation, K = 16
+ * per product, the operand descriptors the attention kernels use) and times
+ * them in SM clock cycles: *cycles to the completion of a final commit,
+ * *issue_cycles (optional) the time the issuing thread spends handing them
+ * over.  group = 0: one run of `count` products; group > 0 (a multiple of 8
+ * dividing count): after every `group` products the thread commits and waits
+ * for them to complete before the next group, the dependent chain of the
+ * kernels (a group's results feed the work the next group needs).
+ * form: 0 M = 128, N = 128 with A and B in shared memory (the
+ * forward's QK^T and most backward products), 1 M = 128, N = 256, 2 M = 128,
+ * N = 128 with A in TMEM (the forward's PV, the backward's dV), 3 M = 128,
+ * N = 64.  Synchronises the stream.  Errors: JFA_ERR_INVALID_ARG,
+ * JFA_ERR_CUDA, JFA_ERR_DEVICE_TIMEOUT (the commit did not arrive within the
+ * kernels' wait limit).
+ */
+int jfa_selftest_mma_cycles(int form, int count, int group, unsigned long long* cycles,
+                            unsigned long long* issue_cycles, void* stream);
+
+/*
  * Plan-free forward and backward: the tensors, the host offsets and the sizes
  * in one call, as a framework op calls attention, with no plan handle and no
  * workspace.  Arguments mean what they mean for jfa_plan_create (kv_offsets

@@ -106,6 +106,22 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+def selftest_mma_cycles(form: int, count: int = 4096, group: int = 0, stream=None) -> tuple[float, float]:
+    """(cycles per product to completion, cycles per product spent issuing) of
+    one form (jfa_selftest_mma_cycles): 0 M128 N128, 1 M128 N256, 2 M128 N128
+    with A in TMEM, 3 M128 N64; count a multiple of 8; group > 0 waits for
+    each group of that many products before issuing the next."""
+    L = lib()
+    fn = L.jfa_selftest_mma_cycles
+    fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_ulonglong),
+                   ctypes.POINTER(ctypes.c_ulonglong), _vp]
+    fn.restype = ctypes.c_int
+    c, ci = ctypes.c_ulonglong(), ctypes.c_ulonglong()
+    _check(fn(form, count, group, ctypes.byref(c), ctypes.byref(ci), _stream(stream)),
+           "jfa_selftest_mma_cycles")
+    return c.value / count, ci.value / count
+
+
 def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> tuple[int, int]:
     """Run the library's bounded-wait self-test (jfa_selftest_wait_timeout):
     returns (status code, measured wait in ns).  JFA_ERR_DEVICE_TIMEOUT (7) is

@@ -37,6 +37,19 @@ def test_wait_timeout_is_reported_and_context_survives(limit_us):
     assert plan.device_status() == 0
 
 
+def test_mma_selftest_rejects_bad_arguments():
+    # argument checks happen before any launch (runs without a GPU)
+    import ctypes
+    L = jfa.lib()
+    c = ctypes.c_ulonglong()
+    assert L.jfa_selftest_mma_cycles(4, 16, 0, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
+    assert L.jfa_selftest_mma_cycles(0, 0, 0, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
+    assert L.jfa_selftest_mma_cycles(0, 12, 0, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
+    assert L.jfa_selftest_mma_cycles(0, 16, 0, None, None, None) == JFA_ERR_INVALID_ARG
+    assert L.jfa_selftest_mma_cycles(0, 16, 12, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
+    assert L.jfa_selftest_mma_cycles(0, 24, 16, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
+
+
 def test_plan_selftest_rejects_bad_arguments():
     # host-side checks only (no plan, bad codes and limits): runs without a GPU
     L = jfa.lib()
