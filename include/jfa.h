@@ -166,6 +166,19 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
  */
 #define JFA_PLAN_FWD_PAIRS 64u
 
+/*
+ * JFA_PLAN_FWD_TWO: run the forward with two query tiles in flight per CTA
+ * where that kernel applies (D = 128, static schedule, no packed tiles):
+ * each schedule tile {b, h, mp, cost} covers query blocks 2 mp and 2 mp + 1
+ * of sequence b -- the list jfa_build_tiles dir 2 gives, over num_ctas CTAs
+ * -- and the CTA alternates between them, so one tile's tensor-core products
+ * run while the other tile's softmax works (the pages' two query tiles per
+ * CTA: alphasignal JFA page, "Specialized warps keep tensor cores busy").
+ * A sequence with an odd number of query blocks leaves its last tile half
+ * empty.  Not with JFA_PLAN_FWD_PAIRS (invalid together).
+ */
+#define JFA_PLAN_FWD_TWO 256u
+
 /* jfa_plan_create with flags (0 = the schedule described above). */
 int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                        int Lq, int D, int num_ctas, unsigned flags, void* stream, jfa_plan_t* out);
@@ -175,8 +188,8 @@ int jfa_plan_destroy(jfa_plan_t plan);
 
 /*
  * Copy a plan's tile schedule to host memory.  dir: 0 forward (the schedule
- * the plan launches: over pair tiles when it runs CTA pairs, see
- * jfa_plan_forward_pairs), 1 backward.
+ * the plan launches: over tiles of two query blocks when it runs CTA pairs or
+ * two tiles per CTA, see jfa_plan_forward_form), 1 backward.
  * tiles_host receives T records of four int32 {b, h, block, cost} grouped by
  * CTA (or pair), cta_ptr_host receives P+1 CSR offsets (P = min(num_ctas, T),
  * or the number of pairs).  Either
@@ -190,6 +203,10 @@ int jfa_plan_tiles(jfa_plan_t plan, int dir, int32_t* tiles_host, int32_t* cta_p
  * and the default rule given with it), 0 when they are dealt on the host.
  * Either pointer may be NULL. */
 int jfa_plan_claims(jfa_plan_t plan, int* fwd, int* bwd);
+
+/* *form = 0 when the plan's forward runs one query tile per CTA, 1 as CTA
+ * pairs (JFA_PLAN_FWD_PAIRS), 2 with two query tiles per CTA (JFA_PLAN_FWD_TWO). */
+int jfa_plan_forward_form(jfa_plan_t plan, int* form);
 
 /* *pairs = 1 when the plan's forward runs as CTA pairs (JFA_PLAN_FWD_PAIRS), else 0. */
 int jfa_plan_forward_pairs(jfa_plan_t plan, int* pairs);

@@ -35,6 +35,7 @@ PLAN_DELTA_IN_TILES = 8  # JFA_PLAN_DELTA_IN_TILES
 PLAN_NO_PACK = 32  # JFA_PLAN_NO_PACK
 PLAN_FWD_PAIRS = 64  # JFA_PLAN_FWD_PAIRS
 PLAN_STATIC = 128  # JFA_PLAN_STATIC
+PLAN_FWD_TWO = 256  # JFA_PLAN_FWD_TWO
 
 
 class JfaError(RuntimeError):
@@ -94,13 +95,15 @@ def lib() -> ctypes.CDLL:
             L.jfa_plan_selftest.argtypes = [_vp, ctypes.c_int, ctypes.c_uint]
             L.jfa_plan_forward_pairs.argtypes = [_vp, _ip]
             L.jfa_plan_claims.argtypes = [_vp, _ip, _ip]
+            L.jfa_plan_forward_form.argtypes = [_vp, _ip]
             L.jfa_status_string.argtypes = [ctypes.c_int]
             L.jfa_status_string.restype = ctypes.c_char_p
             for name in ("jfa_plan_create", "jfa_plan_create_ex", "jfa_plan_destroy", "jfa_plan_tiles", "jfa_build_tiles",
                          "jfa_fwd", "jfa_bwd", "jfa_bwd_preprocess", "jfa_bwd_main",
                          "jfa_plan_device_status", "jfa_delta_in_tiles", "jfa_fwd_simple",
                          "jfa_bwd_simple", "jfa_simple_device_status", "jfa_simple_release",
-                         "jfa_plan_selftest", "jfa_plan_forward_pairs", "jfa_plan_claims"):
+                         "jfa_plan_selftest", "jfa_plan_forward_pairs", "jfa_plan_claims",
+                         "jfa_plan_forward_form"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -234,6 +237,12 @@ class Plan:
         f, b = ctypes.c_int(), ctypes.c_int()
         _check(lib().jfa_plan_claims(self.handle, ctypes.byref(f), ctypes.byref(b)), "jfa_plan_claims")
         return bool(f.value), bool(b.value)
+
+    def forward_form(self) -> int:
+        """0: one query tile per CTA, 1: CTA pairs, 2: two query tiles per CTA."""
+        v = ctypes.c_int()
+        _check(lib().jfa_plan_forward_form(self.handle, ctypes.byref(v)), "jfa_plan_forward_form")
+        return v.value
 
     def forward_pairs(self) -> bool:
         """Whether the plan's forward runs as CTA pairs over pair tiles."""

@@ -179,7 +179,8 @@ bool claims_bwd(unsigned flags, bool broadcast) {
 }
 bool bad_flags(unsigned flags) {
   return ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) ||
-         ((flags & JFA_PLAN_DYNAMIC) && (flags & JFA_PLAN_STATIC));
+         ((flags & JFA_PLAN_DYNAMIC) && (flags & JFA_PLAN_STATIC)) ||
+         ((flags & JFA_PLAN_FWD_PAIRS) && (flags & JFA_PLAN_FWD_TWO));
 }
 
 bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B,
@@ -328,9 +329,14 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   p->fwd_dynamic = claims_fwd(flags);
   p->bwd_dynamic = claims_bwd(flags, p->broadcast);
   p->fwd_pair = use_fwd_pairs(flags, D, p->packed, p->fwd_dynamic, p->num_ctas, qlen);
-  p->fwd = p->fwd_pair ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas / 2, nullptr, false)
-                       : jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr,
-                                                 p->fwd_dynamic);
+  // two query tiles per CTA: where that kernel exists (D = 128, static, no
+  // packed tiles) and there are queries
+  p->fwd_two = (flags & JFA_PLAN_FWD_TWO) && D == 128 && !p->packed && !p->fwd_dynamic &&
+               std::any_of(qlen.begin(), qlen.end(), [](int64_t q) { return q > 0; });
+  p->fwd = p->fwd_pair  ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas / 2, nullptr, false)
+           : p->fwd_two ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas, nullptr, false)
+                        : jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr,
+                                                  p->fwd_dynamic);
   p->bwd = jfa::build_bwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr, p->bwd_dynamic);
   p->own_delta = tiles_form_delta(flags, qlen, kvlen, p->bwd, kv_offsets_host);
   for (int b = 0; b < B; ++b) {
@@ -397,6 +403,12 @@ int jfa_plan_claims(jfa_plan_t plan, int* fwd, int* bwd) {
   if (!plan) return JFA_ERR_INVALID_ARG;
   if (fwd) *fwd = plan->fwd_dynamic ? 1 : 0;
   if (bwd) *bwd = plan->bwd_dynamic ? 1 : 0;
+  return JFA_OK;
+}
+
+int jfa_plan_forward_form(jfa_plan_t plan, int* form) {
+  if (!plan || !form) return JFA_ERR_INVALID_ARG;
+  *form = plan->fwd_pair ? 1 : plan->fwd_two ? 2 : 0;
   return JFA_OK;
 }
 
@@ -471,8 +483,10 @@ int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float 
       return JFA_ERR_CUDA;
   }
   a.pair = plan->fwd_pair;
-  cudaError_t e = jfa::launch_fwd(a, qm, km, vm, om, plan->fwd_pair ? 2 * plan->fwd.P : plan->fwd.P,
-                                  static_cast<cudaStream_t>(stream));
+  cudaError_t e = plan->fwd_two
+                      ? jfa::launch_fwd_two(a, qm, km, vm, om, plan->fwd.P, static_cast<cudaStream_t>(stream))
+                      : jfa::launch_fwd(a, qm, km, vm, om, plan->fwd_pair ? 2 * plan->fwd.P : plan->fwd.P,
+                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
 }
 

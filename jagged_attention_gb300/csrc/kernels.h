@@ -81,6 +81,12 @@ cudaError_t launch_fwd(const FwdArgs& a, const CUtensorMap& q_map, const CUtenso
                        const CUtensorMap& v_map, const CUtensorMap& o_map, int grid,
                        cudaStream_t stream);
 
+// Forward with two query tiles in flight per CTA (D = 128, static schedule
+// over tiles {b, h, mp, cost} of query blocks 2 mp and 2 mp + 1; grid = P).
+cudaError_t launch_fwd_two(const FwdArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                           const CUtensorMap& v_map, const CUtensorMap& o_map, int grid,
+                           cudaStream_t stream);
+
 // Backward pre-pass: delta[h, i] = sum_d dO[i,h,d] * O[i,h,d].
 cudaError_t launch_delta(const uint16_t* out, const uint16_t* dout, float* delta, int64_t n_o,
                          int H, int D, cudaStream_t stream);

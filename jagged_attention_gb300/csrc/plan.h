@@ -66,6 +66,9 @@ struct jfa_plan {
   // the forward runs as CTA pairs over pairs of query blocks; `fwd` then
   // holds the pair schedule, P pairs (2 P CTAs)
   bool fwd_pair = false;
+  // the forward runs two query tiles per CTA; `fwd` then holds the tiles of
+  // two query blocks, over P CTAs
+  bool fwd_two = false;
   // failure-path test only (jfa_plan_selftest)
   int test_skip = 0;
   uint64_t test_limit_ns = 0;

@@ -32,7 +32,7 @@ def test_binding_constants_match_the_header():
     assert flags == {"PACK_SHORT": jfa.PLAN_PACK_SHORT, "DYNAMIC": jfa.PLAN_DYNAMIC,
                      "DELTA_PREPASS": jfa.PLAN_DELTA_PREPASS, "DELTA_IN_TILES": jfa.PLAN_DELTA_IN_TILES,
                      "NO_PACK": jfa.PLAN_NO_PACK, "FWD_PAIRS": jfa.PLAN_FWD_PAIRS,
-                     "STATIC": jfa.PLAN_STATIC}
+                     "STATIC": jfa.PLAN_STATIC, "FWD_TWO": jfa.PLAN_FWD_TWO}
     codes = {int(m[1]): m[0] for m in re.findall(r"\b(JFA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text)}
     assert codes == jfa.STATUS_NAMES
 
@@ -224,6 +224,8 @@ def test_rejects_bad_arguments_before_touching_the_device():
                    flags=jfa.PLAN_DELTA_PREPASS | jfa.PLAN_DELTA_IN_TILES) == 1
     assert _create(ok, None, 2, 1, 4, 128,                           # claimed and dealt
                    flags=jfa.PLAN_DYNAMIC | jfa.PLAN_STATIC) == 1
+    assert _create(ok, None, 2, 1, 4, 128,                           # two forward forms
+                   flags=jfa.PLAN_FWD_PAIRS | jfa.PLAN_FWD_TWO) == 1
     L = jfa.lib()
     T, P = ctypes.c_int(), ctypes.c_int()
     kv = np.array([0, 4, 2], dtype=np.int32)
@@ -234,6 +236,7 @@ def test_rejects_bad_arguments_before_touching_the_device():
                              ctypes.byref(T), ctypes.byref(P)) == 1  # bad direction (0, 1, 2 exist)
     assert L.jfa_plan_forward_pairs(None, None) == 1
     assert L.jfa_plan_claims(None, None, None) == 1
+    assert L.jfa_plan_forward_form(None, None) == 1
     with pytest.raises(jfa.JfaError):
         jfa.build_tiles(kv, None, H=1, Lq=4, num_ctas=8, direction=1, flags=jfa.PLAN_DYNAMIC | jfa.PLAN_STATIC)
     assert L.jfa_fwd(None, None, None, None, 1.0, None, None, None) == 1

@@ -57,7 +57,7 @@ def test_plan_selftest_rejects_bad_arguments():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("skip,flags", [(1, 0), (2, 0), (1, jfa.PLAN_FWD_PAIRS)])
+@pytest.mark.parametrize("skip,flags", [(1, 0), (2, 0), (1, jfa.PLAN_FWD_PAIRS), (1, jfa.PLAN_FWD_TWO)])
 def test_real_kernel_timeout_cascade(skip, flags):
     """One softmax warp of CTA 0 withholds one arrival (skip 1: the forward's
     first P block, 2: the backward's first dS^T), with every wait limited to
@@ -68,12 +68,12 @@ def test_real_kernel_timeout_cascade(skip, flags):
     CTA's roles run out on their own waits (its loads' forwarder, its softmax
     warps) and both CTAs meet at the cluster barrier before releasing TMEM."""
     import torch
-    if flags & jfa.PLAN_FWD_PAIRS:  # D = 128, two query blocks: a pair tile per sequence
+    if flags & (jfa.PLAN_FWD_PAIRS | jfa.PLAN_FWD_TWO):  # D = 128, two query blocks per sequence
         p = parity.to_cuda(workloads.make_problem(3, 2, 128, "broadcast", [300, 5, 128], Lq=256, seed=57))
     else:
         p = parity.to_cuda(workloads.make_workload("tiny_broadcast", seed=0))
     plan = parity.make_plan(p, 0, flags)
-    assert plan.forward_pairs() == bool(flags & jfa.PLAN_FWD_PAIRS)
+    assert plan.forward_form() == (1 if flags & jfa.PLAN_FWD_PAIRS else 2 if flags & jfa.PLAN_FWD_TWO else 0)
     out, lse, _ = parity.gpu_fwd(p, plan)
     plan.selftest(skip, 20000)
     if skip == 1:
