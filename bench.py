@@ -48,6 +48,7 @@ NCU_TRAFFIC = {
     "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2422e+09, "src_hash": "0c0612018e8548c4"},
     "jfa_fwd_kernel:gem_broadcast": {"bytes": 1.7855e+09, "src_hash": "1563cbaeaea90a38"},
     "jfa_fwd_kernel:gem_broadcast:pairs": {"bytes": 1.7879e+09, "src_hash": "1563cbaeaea90a38"},
+    "jfa_fwd_kernel:gem_broadcast:two": {"bytes": 1.7843e+09, "src_hash": "9a7f0418b3ac33a7"},
 }
 
 
@@ -509,7 +510,8 @@ def run_ours(args, rank, world, dist):
     bw_peak = pk["hbm_gbs"]
     per_kernel = {
         "jfa_fwd_kernel": {"ms": k_fwd / args.steps, "flops": flops(prob, "fwd"),
-                           "bytes": alg_bytes(prob, "fwd"), "src": "fwd.cu"},
+                           "bytes": alg_bytes(prob, "fwd"),
+                           "src": "fwd2.cu" if plan.forward_form() == 2 else "fwd.cu"},
         "bwd_preprocess": {"ms": k_pre / args.steps, "flops": 0.0,
                            "bytes": alg_bytes(prob, "pre", pack, own_delta), "src": "bwd.cu"},
         "jfa_bwd_kernel": {"ms": k_main / args.steps, "flops": flops(prob, "bwd"),
@@ -525,8 +527,10 @@ def run_ours(args, rank, world, dist):
     dom = per_kernel[dom_name]
     ridge = tf_peak * 1e12 / (bw_peak * 1e9)
     ai = dom["flops"] / dom["bytes"]
-    # stored counters are per kernel form: the pair forward is its own kernel
-    key = f"{dom_name}:{args.workload}" + (":pairs" if dom_name == "jfa_fwd_kernel" and plan.forward_pairs() else "")
+    # stored counters are per kernel form: the pair and two-tile forwards are
+    # kernels of their own
+    form = {0: "", 1: ":pairs", 2: ":two"}[plan.forward_form()] if dom_name == "jfa_fwd_kernel" else ""
+    key = f"{dom_name}:{args.workload}{form}"
     tr = NCU_TRAFFIC.get(key)
     traffic = tr["bytes"] if tr and tr.get("src_hash") == src_hash(dom["src"]) else None
     if ai >= ridge:
@@ -568,7 +572,7 @@ def run_ours(args, rank, world, dist):
                                    if split else f"dp{world} (independent batches)"),
                    "plan": ("short sequences packed" if pack else "plain schedule")
                            + claims_note(plan)
-                           + (", forward as CTA pairs" if plan.forward_pairs() else ""),
+                           + FORWARD_FORMS[plan.forward_form()],
                    "delta": "formed by the backward tiles" if own_delta else "pre-pass"},
         "fwd_tflops": per_kernel["jfa_fwd_kernel"]["tflops"],
         "bwd_tflops": flops(prob, "bwd") / ((k_pre + k_main) / args.steps * 1e-3) / 1e12,
@@ -592,6 +596,9 @@ def pack_mode(args) -> str:
     return "force" if args.pack else ("off" if args.no_pack else "auto")
 
 
+FORWARD_FORMS = {0: "", 1: ", forward as CTA pairs", 2: ", forward with two query tiles per CTA"}
+
+
 def claims_note(plan) -> str:
     fwd, bwd = plan.claims()
     if fwd and bwd:
@@ -606,7 +613,8 @@ def plan_flags(args, jfa) -> int:
             | (jfa.PLAN_DYNAMIC if args.dynamic else 0) | (jfa.PLAN_STATIC if args.static else 0)
             | (jfa.PLAN_DELTA_PREPASS if args.delta_prepass else 0)
             | (jfa.PLAN_DELTA_IN_TILES if args.delta_in_tiles else 0)
-            | (jfa.PLAN_FWD_PAIRS if args.fwd_pairs else 0))
+            | (jfa.PLAN_FWD_PAIRS if args.fwd_pairs else 0) | (jfa.PLAN_FWD_TWO if args.fwd_two else 0)
+            | (jfa.PLAN_FWD_ONE if args.fwd_one else 0))
 
 
 def run_e2e(args, prob, dev, stream, jfa):
@@ -709,8 +717,13 @@ def main():
                     help="pack short sequences into shared tiles wherever a run forms (by default "
                          "the library packs when that removes an eighth of the tiles)")
     pk.add_argument("--no-pack", action="store_true", help="never pack short sequences")
-    ap.add_argument("--fwd-pairs", action="store_true",
+    fw = ap.add_mutually_exclusive_group()
+    fw.add_argument("--fwd-pairs", action="store_true",
                     help="run the forward as CTA pairs where the plan allows (JFA_PLAN_FWD_PAIRS)")
+    fw.add_argument("--fwd-two", action="store_true",
+                    help="two query tiles per CTA wherever the plan allows (JFA_PLAN_FWD_TWO; by default "
+                         "where tiles are long)")
+    fw.add_argument("--fwd-one", action="store_true", help="one query tile per CTA (JFA_PLAN_FWD_ONE)")
     ap.add_argument("--batch", type=int, default=None,
                     help="keep only the first B sequences of the workload (profiling captures)")
     ap.add_argument("--split-batch", action="store_true",

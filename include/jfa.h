@@ -175,9 +175,15 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
  * run while the other tile's softmax works (the pages' two query tiles per
  * CTA: alphasignal JFA page, "Specialized warps keep tensor cores busy").
  * A sequence with an odd number of query blocks leaves its last tile half
- * empty.  Not with JFA_PLAN_FWD_PAIRS (invalid together).
+ * empty.  By default a plan runs this form where it applies and its tiles
+ * hold at least 3 key blocks on average with at most a quarter of them half
+ * empty (measured faster there, slower on short tiles); JFA_PLAN_FWD_TWO
+ * asks for it wherever it applies, JFA_PLAN_FWD_ONE never.  At most one of
+ * JFA_PLAN_FWD_PAIRS, JFA_PLAN_FWD_TWO and JFA_PLAN_FWD_ONE (invalid
+ * together).
  */
 #define JFA_PLAN_FWD_TWO 256u
+#define JFA_PLAN_FWD_ONE 512u
 
 /* jfa_plan_create with flags (0 = the schedule described above). */
 int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,

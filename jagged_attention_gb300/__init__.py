@@ -36,6 +36,7 @@ PLAN_NO_PACK = 32  # JFA_PLAN_NO_PACK
 PLAN_FWD_PAIRS = 64  # JFA_PLAN_FWD_PAIRS
 PLAN_STATIC = 128  # JFA_PLAN_STATIC
 PLAN_FWD_TWO = 256  # JFA_PLAN_FWD_TWO
+PLAN_FWD_ONE = 512  # JFA_PLAN_FWD_ONE
 
 
 class JfaError(RuntimeError):

@@ -180,7 +180,27 @@ bool claims_bwd(unsigned flags, bool broadcast) {
 bool bad_flags(unsigned flags) {
   return ((flags & JFA_PLAN_PACK_SHORT) && (flags & JFA_PLAN_NO_PACK)) ||
          ((flags & JFA_PLAN_DYNAMIC) && (flags & JFA_PLAN_STATIC)) ||
-         ((flags & JFA_PLAN_FWD_PAIRS) && (flags & JFA_PLAN_FWD_TWO));
+         __builtin_popcount(flags & (JFA_PLAN_FWD_PAIRS | JFA_PLAN_FWD_TWO | JFA_PLAN_FWD_ONE)) > 1;
+}
+
+// Whether the forward runs two query tiles per CTA: on request, or by default
+// where the tiles of two query blocks hold at least 3 key blocks on average
+// and at most a quarter of them have an empty second block; only where that
+// kernel exists (D = 128, static schedule, no packed tiles) and there are
+// queries.
+bool use_fwd_two(unsigned flags, int D, bool packed, bool dynamic, const std::vector<int64_t>& qlen,
+                 const std::vector<int64_t>& kvlen) {
+  if ((flags & (JFA_PLAN_FWD_ONE | JFA_PLAN_FWD_PAIRS)) || D != 128 || packed || dynamic) return false;
+  int64_t tiles = 0, half = 0, blocks = 0;
+  for (size_t b = 0; b < qlen.size(); ++b) {
+    const int64_t nb = (qlen[b] + jfa::kBM - 1) / jfa::kBM, nt = (nb + 1) / 2;
+    tiles += nt;
+    half += nb & 1;
+    blocks += nt * ((kvlen[b] + jfa::kBN - 1) / jfa::kBN);
+  }
+  if (tiles == 0) return false;
+  if (flags & JFA_PLAN_FWD_TWO) return true;
+  return blocks >= 3 * tiles && 4 * half <= tiles;
 }
 
 bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B,
@@ -329,10 +349,7 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   p->fwd_dynamic = claims_fwd(flags);
   p->bwd_dynamic = claims_bwd(flags, p->broadcast);
   p->fwd_pair = use_fwd_pairs(flags, D, p->packed, p->fwd_dynamic, p->num_ctas, qlen);
-  // two query tiles per CTA: where that kernel exists (D = 128, static, no
-  // packed tiles) and there are queries
-  p->fwd_two = (flags & JFA_PLAN_FWD_TWO) && D == 128 && !p->packed && !p->fwd_dynamic &&
-               std::any_of(qlen.begin(), qlen.end(), [](int64_t q) { return q > 0; });
+  p->fwd_two = !p->fwd_pair && use_fwd_two(flags, D, p->packed, p->fwd_dynamic, qlen, kvlen);
   p->fwd = p->fwd_pair  ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas / 2, nullptr, false)
            : p->fwd_two ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas, nullptr, false)
                         : jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr,

@@ -32,7 +32,8 @@ def test_binding_constants_match_the_header():
     assert flags == {"PACK_SHORT": jfa.PLAN_PACK_SHORT, "DYNAMIC": jfa.PLAN_DYNAMIC,
                      "DELTA_PREPASS": jfa.PLAN_DELTA_PREPASS, "DELTA_IN_TILES": jfa.PLAN_DELTA_IN_TILES,
                      "NO_PACK": jfa.PLAN_NO_PACK, "FWD_PAIRS": jfa.PLAN_FWD_PAIRS,
-                     "STATIC": jfa.PLAN_STATIC, "FWD_TWO": jfa.PLAN_FWD_TWO}
+                     "STATIC": jfa.PLAN_STATIC, "FWD_TWO": jfa.PLAN_FWD_TWO,
+                     "FWD_ONE": jfa.PLAN_FWD_ONE}
     codes = {int(m[1]): m[0] for m in re.findall(r"\b(JFA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text)}
     assert codes == jfa.STATUS_NAMES
 
@@ -224,8 +225,9 @@ def test_rejects_bad_arguments_before_touching_the_device():
                    flags=jfa.PLAN_DELTA_PREPASS | jfa.PLAN_DELTA_IN_TILES) == 1
     assert _create(ok, None, 2, 1, 4, 128,                           # claimed and dealt
                    flags=jfa.PLAN_DYNAMIC | jfa.PLAN_STATIC) == 1
-    assert _create(ok, None, 2, 1, 4, 128,                           # two forward forms
-                   flags=jfa.PLAN_FWD_PAIRS | jfa.PLAN_FWD_TWO) == 1
+    for both in (jfa.PLAN_FWD_PAIRS | jfa.PLAN_FWD_TWO, jfa.PLAN_FWD_TWO | jfa.PLAN_FWD_ONE,
+                 jfa.PLAN_FWD_PAIRS | jfa.PLAN_FWD_ONE):                  # two forward forms
+        assert _create(ok, None, 2, 1, 4, 128, flags=both) == 1
     L = jfa.lib()
     T, P = ctypes.c_int(), ctypes.c_int()
     kv = np.array([0, 4, 2], dtype=np.int32)

@@ -32,8 +32,9 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 VARIANTS = {
-    "gem_broadcast": [0, jfa.PLAN_DYNAMIC],
-    "skewed_broadcast": [0],
+    # the default (two query tiles per CTA), one tile per CTA, claimed tiles
+    "gem_broadcast": [0, jfa.PLAN_FWD_ONE, jfa.PLAN_DYNAMIC],
+    "skewed_broadcast": [0, jfa.PLAN_FWD_ONE],
     # unpacked, the default (packed, backward tiles claimed at run time), the
     # same with both passes dealt on the host, both passes claimed
     "block_diag": [jfa.PLAN_NO_PACK, 0, jfa.PLAN_STATIC, jfa.PLAN_DYNAMIC],

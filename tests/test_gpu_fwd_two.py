@@ -49,7 +49,7 @@ def test_two_tiles_match_oracle_and_one_tile(name, num_ctas):
     out, lse, plan = _fwd(p, TWO | jfa.PLAN_NO_PACK, num_ctas)
     assert plan.forward_form() == 2
     parity.check_fwd(out, lse, *parity.oracle_fwd(p))
-    o1, l1, plan1 = _fwd(p, jfa.PLAN_NO_PACK, num_ctas)
+    o1, l1, plan1 = _fwd(p, jfa.PLAN_FWD_ONE | jfa.PLAN_NO_PACK, num_ctas)
     assert plan1.forward_form() == 0
     # the same fp32 arithmetic per row, in the same order: equal bits
     assert torch.equal(out, o1)
@@ -64,8 +64,17 @@ def test_backward_after_two_tile_forward():
 
 
 def test_plan_rule_for_two_tiles():
-    even = parity.to_cuda(CASES["broadcast_256"]())
+    # by default: tiles of two query blocks holding >= 3 key blocks on average,
+    # at most a quarter of them half empty
+    even = parity.to_cuda(CASES["broadcast_256"]())          # 2.5 key blocks per tile
     assert parity.make_plan(even).forward_form() == 0
+    assert parity.make_plan(even, 0, TWO).forward_form() == 2
+    long_ = parity.to_cuda(CASES["broadcast_600"]())         # 2 of 3 tiles per sequence full
+    assert parity.make_plan(long_).forward_form() == 0       # a third half empty
+    gem = parity.to_cuda(CASES["gem_slice"]())
+    assert parity.make_plan(gem).forward_form() == 2
+    assert parity.make_plan(gem, 0, jfa.PLAN_FWD_ONE).forward_form() == 0
+    assert parity.make_plan(gem, 0, jfa.PLAN_FWD_PAIRS).forward_form() == 1
     assert parity.make_plan(even, 0, TWO | jfa.PLAN_DYNAMIC).forward_form() == 0
     d64 = parity.to_cuda(workloads.make_problem(3, 2, 64, "broadcast", [300, 5, 128], Lq=256, seed=65))
     assert parity.make_plan(d64, 0, TWO).forward_form() == 0
