@@ -30,9 +30,13 @@
 //
 // Shared memory: Q_A, Q_B (32 KB each), a two-stage K and V ring (32 KB
 // stages), row statistics.  There is no room left for a separate O staging
-// area, so each tile's O leaves through its own Q buffer at the tile's end
-// (its last products have completed by then), and the next tile's Q load
-// into that buffer waits until O's boxes are read out.
+// area.  At a tile's end both tiles' products on the K and V stages of its
+// last block have completed, and the producer's next loads into those two
+// stages come one block into the next tile: O_A leaves through that K stage
+// and O_B through that V stage, the producer's next load into either waiting
+// until O's boxes have been read out of it.  The Q buffers are released as
+// soon as each tile's last QK^T completes, so the next tile's Q loads run
+// while the softmax warps write O.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 #include "tiles.cuh"
@@ -67,6 +71,7 @@ struct Fwd2Cfg {
 struct Fwd2Bars {
   uint64_t q_full[2], q_free[2];  // per tile slot X (A = 0, B = 1)
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t ko_free[2], vo_free[2];  // per stage: O boxes staged there at a tile end read out
   uint64_t s_full[2], p_full[2], pv_done[2], o_empty[2];
   uint64_t max_ready[2][2][4];  // [slot][buffer][TMEM lane quadrant]
   uint64_t sum_ready[2][2][4];
@@ -106,6 +111,10 @@ __device__ void fwd2_producer(const FwdArgs& a, const CUtensorMap* q_map, const 
   tma_prefetch_desc(k_map);
   tma_prefetch_desc(v_map);
   uint32_t nq[2] = {0, 0}, nk = 0, nv = 0;  // Q loads per slot, K and V loads issued
+  // per stage: an epilogue stages O there (set when a tile's last block is
+  // loaded into it) and the waits done for that so far
+  bool k_held[2] = {false, false}, v_held[2] = {false, false};
+  uint32_t k_waits[2] = {0, 0}, v_waits[2] = {0, 0};
   bool ok = true;
   for (int i = a.cta_ptr[blockIdx.x]; i < a.cta_ptr[blockIdx.x + 1] && ok; ++i) {
     const PTile t = load_ptile(a.tiles, i);
@@ -116,27 +125,37 @@ __device__ void fwd2_producer(const FwdArgs& a, const CUtensorMap* q_map, const 
     auto load_k = [&](int j) -> bool {
       const uint32_t st = nk % C::kStages, ph = (nk / C::kStages) & 1;
       if (!mbar_wait(smem_u32(&bars.k_empty[st]), ph ^ 1, ab)) return false;
+      if (k_held[st]) {  // O_A of an earlier tile leaves through this stage
+        if (!mbar_wait(smem_u32(&bars.ko_free[st]), k_waits[st] & 1, ab)) return false;
+        ++k_waits[st];
+        k_held[st] = false;
+      }
       mbar_arrive_expect_tx(smem_u32(&bars.k_full[st]), C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < 2; ++c)
         tma_load_2d(sbase + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes, k_map,
                     smem_u32(&bars.k_full[st]), x0 + c * 64, kv0 + j * 128);
       ++nk;
+      if (j == t.cost - 1) k_held[st] = true;
       return true;
     };
     auto load_v = [&](int j) -> bool {
       const uint32_t st = nv % C::kStages, ph = (nv / C::kStages) & 1;
       if (!mbar_wait(smem_u32(&bars.v_empty[st]), ph ^ 1, ab)) return false;
+      if (v_held[st]) {  // O_B of an earlier tile leaves through this stage
+        if (!mbar_wait(smem_u32(&bars.vo_free[st]), v_waits[st] & 1, ab)) return false;
+        ++v_waits[st];
+        v_held[st] = false;
+      }
       mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), C::kTileBytes);
 #pragma unroll
       for (int c = 0; c < 2; ++c)
         tma_load_2d(sbase + C::kOffV + st * C::kTileBytes + c * C::kChunkBytes, v_map,
                     smem_u32(&bars.v_full[st]), x0 + c * 64, kv0 + j * 128);
       ++nv;
+      if (j == t.cost - 1) v_held[st] = true;
       return true;
     };
-    // the first K block goes out while the previous tile's O still occupies
-    // the Q buffers
     ok = load_k(0);
     for (int X = 0; X < 2 && ok; ++X) {
       ok = mbar_wait(smem_u32(&bars.q_free[X]), (nq[X] & 1) ^ 1, ab);
@@ -220,9 +239,14 @@ __device__ void fwd2_mma(const FwdArgs& a, uint32_t sbase, uint32_t tmem, Fwd2Ba
     if (t.cost == 0) continue;
     ok = mbar_wait(smem_u32(&bars.q_full[X]), tq & 1, ab);
     if (ok) ok = issue_s(g);
+    // Q_X is free for the next tile once this tile's last QK^T has completed
+    if (ok && t.cost == 1) mma_commit(smem_u32(&bars.q_free[X]));
     for (int j = 0; j < t.cost && ok; ++j) {
       ok = issue_pv(g + j, j == 0);
-      if (ok && j + 1 < t.cost) ok = issue_s(g + j + 1);
+      if (ok && j + 1 < t.cost) {
+        ok = issue_s(g + j + 1);
+        if (ok && j + 2 == t.cost) mma_commit(smem_u32(&bars.q_free[X]));
+      }
     }
     g += t.cost;
     ++tq;
@@ -347,9 +371,9 @@ __device__ void fwd2_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t
       }
     }
     // epilogues: combine the groups' row sums, wait for the tile's last PV,
-    // normalise this group's O columns and store them through the tile's Q
-    // buffer (its products have completed), then hand the buffer back
-    const uint32_t gl = g + t.cost - 1;
+    // normalise this group's O columns and store them through the K (tile A)
+    // or V (tile B) stage of the last block, then hand the stage back
+    const uint32_t gl = g + t.cost - 1, sl = gl % C::kStages;
 #pragma unroll
     for (int X = 0; X < 2; ++X) {
       float* xs = xsum + ((X * 2 + (tq & 1)) * 2) * 256;  // [group][exact, rounded][128]
@@ -372,7 +396,8 @@ __device__ void fwd2_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t
       // a warp whose 32 rows all belong to the sequence stores them as one
       // swizzled box through the Q buffer; others store their valid rows
       const bool staged = __all_sync(0xffffffffu, row_ok[X]);
-      const uint32_t stg = smem_u32(smem + C::kOffQ + X * C::kTileBytes) + grp * C::kChunkBytes + wq * 4096;
+      const uint32_t stg = smem_u32(smem + (X == 0 ? C::kOffK : C::kOffV) + sl * C::kTileBytes) +
+                           grp * C::kChunkBytes + wq * 4096;
       uint16_t* orow_ptr = a.out + (orow * H + t.h) * D + c0;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -397,9 +422,9 @@ __device__ void fwd2_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t
         if (staged) {
           tma_store_2d(o_map, stg, t.h * D + c0, static_cast<int>(orow - lane));
           bulk_commit();
-          bulk_wait_read_all();  // the box has left the Q buffer
+          bulk_wait_read_all();  // the box has left the stage
         }
-        mbar_arrive(smem_u32(&bars.q_free[X]));
+        mbar_arrive(smem_u32(X == 0 ? &bars.ko_free[sl] : &bars.vo_free[sl]));
       }
       if (row_ok[X] && grp == 0) a.lse[int64_t(t.h) * a.pb.n_o + orow] = (m_run[X] + __log2f(l_all)) * kLn2f;
     }
@@ -422,7 +447,9 @@ __global__ void __launch_bounds__(Fwd2Cfg::kThreads, 1)
   if (tid == 0) {
     for (int X = 0; X < 2; ++X) {
       mbar_init(smem_u32(&bars.q_full[X]), 1);
-      mbar_init(smem_u32(&bars.q_free[X]), 8);  // lane 0 of each softmax warp
+      mbar_init(smem_u32(&bars.q_free[X]), 1);   // slot X's issuer
+      mbar_init(smem_u32(&bars.ko_free[X]), 8);  // lane 0 of each softmax warp (stage X)
+      mbar_init(smem_u32(&bars.vo_free[X]), 8);
       mbar_init(smem_u32(&bars.k_full[X]), 1);
       mbar_init(smem_u32(&bars.k_empty[X]), 2);  // both issuers
       mbar_init(smem_u32(&bars.v_full[X]), 1);
