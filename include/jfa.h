@@ -175,9 +175,10 @@ int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
  * run while the other tile's softmax works (the pages' two query tiles per
  * CTA: alphasignal JFA page, "Specialized warps keep tensor cores busy").
  * A sequence with an odd number of query blocks leaves its last tile half
- * empty.  By default a plan runs this form where it applies and its tiles
+ * empty.  By default a plan runs this form where it applies, its tiles
  * hold at least 3 key blocks on average with at most a quarter of them half
- * empty (measured faster there, slower on short tiles); JFA_PLAN_FWD_TWO
+ * empty, and there are at least four of them per CTA (measured faster there,
+ * slower on short tiles and on few tiles per CTA); JFA_PLAN_FWD_TWO
  * asks for it wherever it applies, JFA_PLAN_FWD_ONE never.  At most one of
  * JFA_PLAN_FWD_PAIRS, JFA_PLAN_FWD_TWO and JFA_PLAN_FWD_ONE (invalid
  * together).
@@ -377,10 +378,12 @@ int jfa_selftest_wait_timeout(unsigned limit_us, unsigned long long* waited_ns, 
  * dividing count): after every `group` products the thread commits and waits
  * for them to complete before the next group, the dependent chain of the
  * kernels (a group's results feed the work the next group needs).
- * form: 0 M = 128, N = 128 with A and B in shared memory (the
- * forward's QK^T and most backward products), 1 M = 128, N = 256, 2 M = 128,
- * N = 128 with A in TMEM (the forward's PV, the backward's dV), 3 M = 128,
- * N = 64.  Synchronises the stream.  Errors: JFA_ERR_INVALID_ARG,
+ * form: 0 M = 128, N = 128 with A and B in shared memory, both K-major (the
+ * forward's QK^T, the backward's S^T and dP^T), 1 M = 128, N = 256, 2 M = 128,
+ * N = 128 with A in TMEM, 3 M = 128, N = 64, 4 as 0 with B MN-major (the
+ * backward's dK), 5 as 0 with A and B MN-major (the backward's dQ), 6 as 2
+ * with B MN-major (the forward's PV, the backward's dV).  Synchronises the
+ * stream.  Errors: JFA_ERR_INVALID_ARG,
  * JFA_ERR_CUDA, JFA_ERR_DEVICE_TIMEOUT (the commit did not arrive within the
  * kernels' wait limit).
  */

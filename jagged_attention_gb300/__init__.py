@@ -113,8 +113,9 @@ def lib() -> ctypes.CDLL:
 def selftest_mma_cycles(form: int, count: int = 4096, group: int = 0, stream=None) -> tuple[float, float]:
     """(cycles per product to completion, cycles per product spent issuing) of
     one form (jfa_selftest_mma_cycles): 0 M128 N128, 1 M128 N256, 2 M128 N128
-    with A in TMEM, 3 M128 N64; count a multiple of 8; group > 0 waits for
-    each group of that many products before issuing the next."""
+    with A in TMEM, 3 M128 N64, 4 form 0 with B MN-major, 5 form 0 with A and
+    B MN-major, 6 form 2 with B MN-major; count a multiple of 8; group > 0
+    waits for each group of that many products before issuing the next."""
     L = lib()
     fn = L.jfa_selftest_mma_cycles
     fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_ulonglong),

@@ -188,8 +188,8 @@ bool bad_flags(unsigned flags) {
 // and at most a quarter of them have an empty second block; only where that
 // kernel exists (D = 128, static schedule, no packed tiles) and there are
 // queries.
-bool use_fwd_two(unsigned flags, int D, bool packed, bool dynamic, const std::vector<int64_t>& qlen,
-                 const std::vector<int64_t>& kvlen) {
+bool use_fwd_two(unsigned flags, int D, int H, bool packed, bool dynamic, int num_ctas,
+                 const std::vector<int64_t>& qlen, const std::vector<int64_t>& kvlen) {
   if ((flags & (JFA_PLAN_FWD_ONE | JFA_PLAN_FWD_PAIRS)) || D != 128 || packed || dynamic) return false;
   int64_t tiles = 0, half = 0, blocks = 0;
   for (size_t b = 0; b < qlen.size(); ++b) {
@@ -200,7 +200,9 @@ bool use_fwd_two(unsigned flags, int D, bool packed, bool dynamic, const std::ve
   }
   if (tiles == 0) return false;
   if (flags & JFA_PLAN_FWD_TWO) return true;
-  return blocks >= 3 * tiles && 4 * half <= tiles;
+  // fewer than four tiles per CTA: halving the tile count costs more balance
+  // than the second tile gains (jagged self, ~2 per CTA, measured 5% slower)
+  return blocks >= 3 * tiles && 4 * half <= tiles && tiles * H >= 4 * int64_t(num_ctas);
 }
 
 bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B,
@@ -349,7 +351,7 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   p->fwd_dynamic = claims_fwd(flags);
   p->bwd_dynamic = claims_bwd(flags, p->broadcast);
   p->fwd_pair = use_fwd_pairs(flags, D, p->packed, p->fwd_dynamic, p->num_ctas, qlen);
-  p->fwd_two = !p->fwd_pair && use_fwd_two(flags, D, p->packed, p->fwd_dynamic, qlen, kvlen);
+  p->fwd_two = !p->fwd_pair && use_fwd_two(flags, D, H, p->packed, p->fwd_dynamic, p->num_ctas, qlen, kvlen);
   p->fwd = p->fwd_pair  ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas / 2, nullptr, false)
            : p->fwd_two ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas, nullptr, false)
                         : jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr,

@@ -83,9 +83,14 @@ __global__ void __launch_bounds__(128, 1) jfa_selftest_mma_kernel(int count, int
   jfa::tc_fence_after();
   if (threadIdx.x == 0) {
     const uint32_t sA = jfa::smem_u32(sm), sB = jfa::smem_u32(sm + 16384);
-    const uint64_t ad = jfa::smem_desc_sw128(sA, 16, 1024), bd = jfa::smem_desc_sw128(sB, 16, 1024);
+    // forms 4-6 read A and / or B in the MN-major layout (64-element chunks
+    // along M / N, 8 KB apart), as the kernels' transposed operands do
+    constexpr bool kAmn = kForm == 5, kBmn = kForm >= 4;
+    const uint64_t ad = jfa::smem_desc_sw128(sA, kAmn ? 8192 : 16, 1024);
+    const uint64_t bd = jfa::smem_desc_sw128(sB, kBmn ? 8192 : 16, 1024);
     constexpr int N = kForm == 1 ? 256 : kForm == 3 ? 64 : 128;
-    constexpr uint32_t id = jfa::idesc_bf16_f32(128, N, false, false);
+    constexpr uint32_t id = jfa::idesc_bf16_f32(128, N, kAmn, kBmn);
+    constexpr bool kTs = kForm == 2 || kForm == 6;
     const jfa::Abort ab{&flag, &g_selftest_status};
     const int G = group > 0 ? group : count;  // both multiples of 8 (checked on the host)
     uint32_t phase = 0;
@@ -95,11 +100,11 @@ __global__ void __launch_bounds__(128, 1) jfa_selftest_mma_kernel(int count, int
     for (int g0 = 0; g0 < count && done; g0 += G) {
       const long long ti = clock64();
       // the first product of the run overwrites the accumulator
-      if constexpr (kForm == 2) jfa::mma_bf16_ts(tm, tm + 384, bd, id, g0 > 0 ? 1u : 0u);
+      if constexpr (kTs) jfa::mma_bf16_ts(tm, tm + 384, bd, id, g0 > 0 ? 1u : 0u);
       else jfa::mma_bf16_ss(tm, ad, bd, id, g0 > 0 ? 1u : 0u);
 #pragma unroll 8
       for (int i = 1; i < G; ++i) {
-        if constexpr (kForm == 2) jfa::mma_bf16_ts(tm, tm + 384, bd, id, 1u);
+        if constexpr (kTs) jfa::mma_bf16_ts(tm, tm + 384, bd, id, 1u);
         else jfa::mma_bf16_ss(tm, ad, bd, id, 1u);
       }
       issue += clock64() - ti;
@@ -133,7 +138,7 @@ cudaError_t launch_mma_selftest(int count, int group, int smem, cudaStream_t s) 
 
 extern "C" int jfa_selftest_mma_cycles(int form, int count, int group, unsigned long long* cycles,
                                        unsigned long long* issue_cycles, void* stream) {
-  if (form < 0 || form > 3 || count < 8 || count > (1 << 20) || count % 8 != 0 || !cycles)
+  if (form < 0 || form > 6 || count < 8 || count > (1 << 20) || count % 8 != 0 || !cycles)
     return JFA_ERR_INVALID_ARG;
   if (group < 0 || (group > 0 && (group % 8 != 0 || count % group != 0))) return JFA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -145,7 +150,10 @@ extern "C" int jfa_selftest_mma_cycles(int form, int count, int group, unsigned 
   const cudaError_t e = form == 0 ? launch_mma_selftest<0>(count, group, smem, s)
                         : form == 1 ? launch_mma_selftest<1>(count, group, smem, s)
                         : form == 2 ? launch_mma_selftest<2>(count, group, smem, s)
-                                    : launch_mma_selftest<3>(count, group, smem, s);
+                        : form == 3 ? launch_mma_selftest<3>(count, group, smem, s)
+                        : form == 4 ? launch_mma_selftest<4>(count, group, smem, s)
+                        : form == 5 ? launch_mma_selftest<5>(count, group, smem, s)
+                                    : launch_mma_selftest<6>(count, group, smem, s);
   if (e != cudaSuccess) return JFA_ERR_CUDA;
   int status = 0;
   unsigned long long c = 0, ci = 0;

@@ -42,7 +42,7 @@ def test_mma_selftest_rejects_bad_arguments():
     import ctypes
     L = jfa.lib()
     c = ctypes.c_ulonglong()
-    assert L.jfa_selftest_mma_cycles(4, 16, 0, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
+    assert L.jfa_selftest_mma_cycles(7, 16, 0, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
     assert L.jfa_selftest_mma_cycles(0, 0, 0, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
     assert L.jfa_selftest_mma_cycles(0, 12, 0, ctypes.byref(c), None, None) == JFA_ERR_INVALID_ARG
     assert L.jfa_selftest_mma_cycles(0, 16, 0, None, None, None) == JFA_ERR_INVALID_ARG

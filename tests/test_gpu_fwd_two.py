@@ -65,16 +65,17 @@ def test_backward_after_two_tile_forward():
 
 def test_plan_rule_for_two_tiles():
     # by default: tiles of two query blocks holding >= 3 key blocks on average,
-    # at most a quarter of them half empty
+    # at most a quarter of them half empty, at least four of them per CTA
     even = parity.to_cuda(CASES["broadcast_256"]())          # 2.5 key blocks per tile
     assert parity.make_plan(even).forward_form() == 0
     assert parity.make_plan(even, 0, TWO).forward_form() == 2
     long_ = parity.to_cuda(CASES["broadcast_600"]())         # 2 of 3 tiles per sequence full
     assert parity.make_plan(long_).forward_form() == 0       # a third half empty
-    gem = parity.to_cuda(CASES["gem_slice"]())
-    assert parity.make_plan(gem).forward_form() == 2
-    assert parity.make_plan(gem, 0, jfa.PLAN_FWD_ONE).forward_form() == 0
-    assert parity.make_plan(gem, 0, jfa.PLAN_FWD_PAIRS).forward_form() == 1
+    gem = parity.to_cuda(CASES["gem_slice"]())               # 256 two-block tiles
+    assert parity.make_plan(gem, 16).forward_form() == 2     # 16 per CTA
+    assert parity.make_plan(gem, 152).forward_form() == 0    # under 4 per CTA
+    assert parity.make_plan(gem, 16, jfa.PLAN_FWD_ONE).forward_form() == 0
+    assert parity.make_plan(gem, 16, jfa.PLAN_FWD_PAIRS).forward_form() == 1
     assert parity.make_plan(even, 0, TWO | jfa.PLAN_DYNAMIC).forward_form() == 0
     d64 = parity.to_cuda(workloads.make_problem(3, 2, 64, "broadcast", [300, 5, 128], Lq=256, seed=65))
     assert parity.make_plan(d64, 0, TWO).forward_form() == 0
