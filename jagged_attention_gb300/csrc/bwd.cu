@@ -52,7 +52,9 @@ __global__ void __launch_bounds__(256)
 //   S^T   = K_n Q_m^T                  tcgen05.mma -> TMEM (kv rows = lanes)
 //   dP^T  = V_n dO_m^T                 tcgen05.mma -> TMEM
 //   P^T   = exp2(c S^T - LSE*log2 e)   WG0, written back to TMEM as bf16
-//   dS^T  = P^T o (dP^T - Delta)       WG0, written to swizzled shared memory
+//   dS^T  = P^T o (dP^T - Delta)       WG0, written to swizzled shared memory,
+//                                      times the softmax scale (which dQ and
+//                                      dK carry: the drain multiplies neither)
 //   dV   += P^T dO_m                   A = P^T from TMEM
 //   dK   += dS^T Q_m                   A = dS^T, K-major view
 //   dQ_m  = dS K_n                     A = the same dS^T buffer, M-major view
@@ -340,16 +342,16 @@ __device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem
     }
     const int64_t o_base = a.pb.q_off ? a.pb.q_off[t.b] : int64_t(t.b) * a.pb.Lq;
     for (int m = 0; m < t.qblocks; ++m, ++gm) {
-      // this group's 64 LSE (log2 units) and Delta values, masked past the
-      // sequence; mbarriers (bounded waits) rather than hardware barriers, so a
-      // timed-out warp can never strand the others
+      // this group's 64 LSE (log2 units) and -scale * Delta values, masked
+      // past the sequence; mbarriers (bounded waits) rather than hardware
+      // barriers, so a timed-out warp can never strand the others
       if (!warp_wait_b(lse_done, (gm & 1) ^ 1, ab)) return;  // previous block's values read
       if (r < 64) {
         const int64_t q = int64_t(m) * 128 + c0 + r;
         const bool q_ok = q < qlen;
         const int64_t idx = int64_t(t.h) * a.pb.n_o + o_base + q;
         lse2[c0 + r] = q_ok ? -(a.lse[idx] * 1.4426950408889634f) : -INFINITY;  // -LSE, log2 units
-        if constexpr (!kOwnDelta) dlt[c0 + r] = q_ok ? a.delta[idx] : 0.0f;
+        if constexpr (!kOwnDelta) dlt[c0 + r] = q_ok ? -(a.scale * a.delta[idx]) : 0.0f;
       }
       mbar_arrive(lse_ready);
       if (!warp_wait_b(lse_ready, gm & 1, ab)) return;
@@ -442,7 +444,7 @@ __device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem
         }
         mbar_arrive(smem_u32(&bars.dsum_part[g]));
         if (!warp_wait_b(smem_u32(&bars.dsum_part[g]), gm & 1, ab)) return;
-        if (r < 64) dlt[c0 + r] = (part[r] + part[64 + r]) + (part[128 + r] + part[192 + r]);
+        if (r < 64) dlt[c0 + r] = -(a.scale * ((part[r] + part[64 + r]) + (part[128 + r] + part[192 + r])));
         mbar_arrive(smem_u32(&bars.dsum_ready[g]));
         if (!warp_wait_b(smem_u32(&bars.dsum_ready[g]), gm & 1, ab)) return;
       }
@@ -461,17 +463,20 @@ __device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem
         // Key rows past the sequence get dS^T = 0 (it reaches dQ through K);
         // their P^T is left unmasked, since it only reaches rows of dV and dK
         // that are never stored.
+        // scale * dS^T = P^T o (scale dP^T - scale Delta): one packed fma in
+        // place of the subtraction
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = 0u;
         if (kv_ok) {
+          const uint64_t sc2 = f2_pack(a.scale, a.scale);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = c0 + c * 32 + 2 * e;
             const uint32_t pp = p[c * 16 + e];
             float d0, d1;
             f2_unpack(f2_mul(f2_pack(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u)),
-                             f2_sub(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                             f2_fma(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2,
                                     *reinterpret_cast<const uint64_t*>(dlt + j))),
                       d0, d1);
             w[e] = pack_bf16x2(d0, d1);
@@ -517,12 +522,12 @@ __device__ __forceinline__ bool key_row_ok(const BwdArgs& a, const BTile& t, int
 }
 
 // 32 dQ columns of one row: reduce-added, or stored when this tile owns the row.
-__device__ __forceinline__ void dq_row_out(float* row, const uint32_t (&v)[32], float scale, bool store) {
+__device__ __forceinline__ void dq_row_out(float* row, const uint32_t (&v)[32], bool store) {
   float4* dst = reinterpret_cast<float4*>(row);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const float4 val = make_float4(__uint_as_float(v[4 * e]) * scale, __uint_as_float(v[4 * e + 1]) * scale,
-                                   __uint_as_float(v[4 * e + 2]) * scale, __uint_as_float(v[4 * e + 3]) * scale);
+    const float4 val = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
     if (store) dst[e] = val;
     else atomicAdd(dst + e, val);
   }
@@ -584,13 +589,9 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
           const uint32_t dst = dst_box + lane * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            st_shared_v4(dst + ((u ^ (lane & 7)) << 4),
-                         __float_as_uint(__uint_as_float(v[4 * u]) * a.scale),
-                         __float_as_uint(__uint_as_float(v[4 * u + 1]) * a.scale),
-                         __float_as_uint(__uint_as_float(v[4 * u + 2]) * a.scale),
-                         __float_as_uint(__uint_as_float(v[4 * u + 3]) * a.scale));
+            st_shared_v4(dst + ((u ^ (lane & 7)) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         } else if (q_ok) {
-          dq_row_out(row + k * 32, v, a.scale, store);
+          dq_row_out(row + k * 32, v, store);
         }
       };
       const int y = static_cast<int>(q_base + int64_t(m) * 128 + wq * 32);
@@ -602,11 +603,13 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
 #pragma unroll
         for (int k2 = 0; k2 < D / 32; k2 += 2) {
           load_pair(k2);
+          if (k2 + 2 == D / 32) {  // every TMEM read of dQ done: its columns are free for the next dP
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.dq_empty));
+          }
           put(k2, box_addr(k2), vv[0]);
           put(k2 + 1, box_addr(k2 + 1), vv[1]);
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.dq_empty));  // dQ TMEM columns free for the next dP
         if (whole) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -633,12 +636,14 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
 #pragma unroll
         for (int k2 = 0; k2 < D / 32; k2 += 2) {
           load_pair(k2);
+          if (k2 + 2 == D / 32) {  // every TMEM read of dQ done
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.dq_empty));
+          }
           const uint32_t base = k2 < kHalf ? do_box + k2 * 16384 : ds_box + (k2 - kHalf) * 16384;
           put(k2, base, vv[0]);
           put(k2 + 1, kHalf == 1 ? ds_box : base + 16384, vv[1]);
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.dq_empty));
         if (whole) fence_proxy_async_smem();
         __syncwarp();
         if (whole && lane == 0) {  // group 1: the dO-half boxes, group 2: the dS^T-buffer boxes
@@ -685,14 +690,14 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
             put_bf16(qh, dv_row, c2 + h, pk);
           }
         }
-        uint32_t dkp[D / 32][16];  // scale * dK of this row, bf16 pairs
+        uint32_t dkp[D / 32][16];  // dK of this row (dS^T carried the scale), bf16 pairs
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t w[32];
           tmem_ld_x32(tl + C::kColDK + c * 32, w);
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            dkp[c][e] = pack_bf16x2(__uint_as_float(w[2 * e]) * a.scale, __uint_as_float(w[2 * e + 1]) * a.scale);
+            dkp[c][e] = pack_bf16x2(__uint_as_float(w[2 * e]), __uint_as_float(w[2 * e + 1]));
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.dkv_empty));  // dV / dK columns free for the next tile
