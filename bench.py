@@ -586,7 +586,7 @@ def run_ours(args, rank, world, dist):
         "cpu_baseline": cpu,
         "e2e": None if e2e is None else {k: e2e[k] for k in
                                           ("value", "unit", "h2d_bytes_per_step",
-                                           "d2h_bytes_per_step", "ms_per_step")},
+                                           "d2h_bytes_per_step", "ms_per_step", "steps")},
         "gpu_launches": (2 if own_delta else 3) * args.steps,  # fwd, [Delta], bwd main
         "clocks": clk.summary(),
         "device_status": status,
@@ -693,7 +693,8 @@ def run_e2e(args, prob, dev, stream, jfa):
     for pl in plans:
         pl.close()
     return {"unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms, "pipelined": "uploads, kernels and downloads of consecutive steps overlap"}
+            "ms_per_step": ms, "steps": n,
+            "pipelined": "uploads, kernels and downloads of consecutive steps overlap"}
 
 
 def main():
@@ -731,7 +732,8 @@ def main():
     ap.add_argument("--split-batch", action="store_true",
                     help="under torchrun: split one batch across the ranks by sequence (strong "
                          "scaling; broadcast mode sums dQ over the ranks) instead of one batch per rank")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=10,
+                    help="timed end-to-end steps (30 measured the same per-step time as 10)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -13,30 +13,43 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Delta_i = sum_d dO_id O_id for every (row, head): the row sum the backward
 // subtracts inside dS = P o (dP - Delta) (the "Di" preprocessing of the TLX
 // Block Attention page, "One Constraint, Five Eliminations").  D/8 lanes per
-// row, 16-byte loads, a shuffle reduction; memory-bound.
+// row, 16-byte loads, a shuffle reduction; memory-bound, so each thread loads
+// the pieces of two rows (one grid stride apart) before reducing either, to
+// keep twice the bytes in flight.
+__device__ __forceinline__ float dot_bf16x8(const uint4& o, const uint4& g) {
+  return bf16_lo(o.x) * bf16_lo(g.x) + bf16_hi(o.x) * bf16_hi(g.x) + bf16_lo(o.y) * bf16_lo(g.y) +
+         bf16_hi(o.y) * bf16_hi(g.y) + bf16_lo(o.z) * bf16_lo(g.z) + bf16_hi(o.z) * bf16_hi(g.z) +
+         bf16_lo(o.w) * bf16_lo(g.w) + bf16_hi(o.w) * bf16_hi(g.w);
+}
+
 __global__ void __launch_bounds__(256)
     delta_kernel(const uint16_t* __restrict__ out, const uint16_t* __restrict__ dout,
                  float* __restrict__ delta, int64_t n_o, int H, int D) {
   const int lanes = D / 8;
   const int64_t rows = n_o * H;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  // the whole warp iterates while any of its lanes has a piece (the shuffles need all lanes)
   for (int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; gid - (threadIdx.x & 31) < rows * lanes;
-       gid += stride) {
-    const int64_t row = gid / lanes;  // row * H + head, in memory order
-    const int sub = static_cast<int>(gid % lanes);
-    float acc = 0.0f;
-    if (row < rows) {
-      const uint4 o = *reinterpret_cast<const uint4*>(out + row * D + sub * 8);
-      const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + sub * 8);
-      acc = bf16_lo(o.x) * bf16_lo(g.x) + bf16_hi(o.x) * bf16_hi(g.x) + bf16_lo(o.y) * bf16_lo(g.y) +
-            bf16_hi(o.y) * bf16_hi(g.y) + bf16_lo(o.z) * bf16_lo(g.z) + bf16_hi(o.z) * bf16_hi(g.z) +
-            bf16_lo(o.w) * bf16_lo(g.w) + bf16_hi(o.w) * bf16_hi(g.w);
+       gid += 2 * stride) {
+    const int64_t row0 = gid / lanes, row1 = (gid + stride) / lanes;
+    const int sub = static_cast<int>(gid % lanes);  // the same for both: stride is a multiple of lanes
+    uint4 o0 = make_uint4(0, 0, 0, 0), g0 = o0, o1 = o0, g1 = o0;
+    if (row0 < rows) {
+      o0 = *reinterpret_cast<const uint4*>(out + row0 * D + sub * 8);
+      g0 = *reinterpret_cast<const uint4*>(dout + row0 * D + sub * 8);
     }
-    for (int w = lanes / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w, lanes);
-    if (sub == 0 && row < rows) {
-      const int64_t i = row / H;
-      const int h = static_cast<int>(row % H);
-      delta[int64_t(h) * n_o + i] = acc;
+    if (row1 < rows) {
+      o1 = *reinterpret_cast<const uint4*>(out + row1 * D + sub * 8);
+      g1 = *reinterpret_cast<const uint4*>(dout + row1 * D + sub * 8);
+    }
+    float acc0 = dot_bf16x8(o0, g0), acc1 = dot_bf16x8(o1, g1);
+    for (int w = lanes / 2; w > 0; w >>= 1) {
+      acc0 += __shfl_xor_sync(0xffffffffu, acc0, w, lanes);
+      acc1 += __shfl_xor_sync(0xffffffffu, acc1, w, lanes);
+    }
+    if (sub == 0) {
+      if (row0 < rows) delta[int64_t(row0 % H) * n_o + row0 / H] = acc0;
+      if (row1 < rows) delta[int64_t(row1 % H) * n_o + row1 / H] = acc1;
     }
   }
 }
