@@ -622,16 +622,27 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
           }
           put(k2, box_addr(k2), vv[0]);
           put(k2 + 1, box_addr(k2 + 1), vv[1]);
+          // these two boxes' reduce-adds start while the next pair is read
+          // (packed plans, whose tiles hold one step each, send all at once)
+          if (!kPack && whole) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              send(k2, box_addr(k2));
+              send(k2 + 1, box_addr(k2 + 1));
+              bulk_commit();
+            }
+          }
         }
-        if (whole) fence_proxy_async_smem();
+        if (kPack && whole) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (whole) {
+          if (kPack && whole) {
 #pragma unroll
             for (int k = 0; k < D / 32; ++k) send(k, box_addr(k));
             bulk_commit();
-            bulk_wait_read_all();
           }
+          if (whole) bulk_wait_read_all();
           mbar_arrive(smem_u32(&bars.q_empty[qs]));
         }
       } else {
@@ -656,16 +667,31 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
           const uint32_t base = k2 < kHalf ? do_box + k2 * 16384 : ds_box + (k2 - kHalf) * 16384;
           put(k2, base, vv[0]);
           put(k2 + 1, kHalf == 1 ? ds_box : base + 16384, vv[1]);
+          if constexpr (D == 128 && !kPack) {
+            // one pair = one half: group 1 (the dO-half boxes) leaves while the
+            // second pair is read, group 2 (the dS^T-buffer boxes) after it
+            if (whole) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                send(k2, base);
+                send(k2 + 1, base + 16384);
+                bulk_commit();
+              }
+            }
+          }
         }
-        if (whole) fence_proxy_async_smem();
-        __syncwarp();
-        if (whole && lane == 0) {  // group 1: the dO-half boxes, group 2: the dS^T-buffer boxes
+        if constexpr (D != 128 || kPack) {
+          if (whole) fence_proxy_async_smem();
+          __syncwarp();
+          if (whole && lane == 0) {  // group 1: the dO-half boxes, group 2: the dS^T-buffer boxes
 #pragma unroll
-          for (int j = 0; j < kHalf; ++j) send(j, do_box + j * 16384);
-          bulk_commit();
+            for (int j = 0; j < kHalf; ++j) send(j, do_box + j * 16384);
+            bulk_commit();
 #pragma unroll
-          for (int j = 0; j < kHalf; ++j) send(kHalf + j, ds_box + j * 16384);
-          bulk_commit();
+            for (int j = 0; j < kHalf; ++j) send(kHalf + j, ds_box + j * 16384);
+            bulk_commit();
+          }
         }
         // dV through the Q half (group 3), dK into registers
         const bool kv_ok = key_row_ok<kPack>(a, t, r);
