@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # 256-sequence capture of the same kernel, scaled by K/V tokens: x3.730),
 # keyed by kernel and workload, valid only while the kernel source hash matches.
 NCU_TRAFFIC = {
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2415e+09, "src_hash": "1bb43be99af9cd27"},
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2421e+09, "src_hash": "df55b77c5dfbab62"},
     "jfa_fwd2_kernel:gem_broadcast": {"bytes": 1.7841e+09, "src_hash": "6d874a31595e22c6"},
 }
 

@@ -613,6 +613,18 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
         else tma_reduce_add_2d(dq_map, src_box, t.h * D + k * 32, y);
       };
       if (!last) {
+        // a staged pair of boxes goes to its reduce-adds while the next pair
+        // is staged (packed plans, whose tiles hold one step each, send all
+        // four at once); TMEM is read and released first
+        auto send_pair = [&](int k2) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            send(k2, box_addr(k2));
+            send(k2 + 1, box_addr(k2 + 1));
+            bulk_commit();
+          }
+        };
 #pragma unroll
         for (int k2 = 0; k2 < D / 32; k2 += 2) {
           load_pair(k2);
@@ -620,20 +632,11 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.dq_empty));
           }
+          if (!kPack && whole && k2 > 0) send_pair(k2 - 2);
           put(k2, box_addr(k2), vv[0]);
           put(k2 + 1, box_addr(k2 + 1), vv[1]);
-          // these two boxes' reduce-adds start while the next pair is read
-          // (packed plans, whose tiles hold one step each, send all at once)
-          if (!kPack && whole) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              send(k2, box_addr(k2));
-              send(k2 + 1, box_addr(k2 + 1));
-              bulk_commit();
-            }
-          }
         }
+        if (!kPack && whole) send_pair(D / 32 - 2);
         if (kPack && whole) fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -657,6 +660,18 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
         const uint32_t do_box = sbase + C::kOffDO + qs * C::kTileBytes + wq * 4096;  // box j at + j * 16384
         const uint32_t ds_box = sbase + C::kOffDS + wq * 4096;
         constexpr int kHalf = D / 64;  // dQ boxes per half
+        // D = 128 (unpacked): one pair = one half.  Group 1 (the dO-half
+        // boxes) leaves once TMEM is read and released, while the second pair
+        // is staged; group 2 (the dS^T-buffer boxes) after it
+        auto send_half = [&](int k2, uint32_t base) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            send(k2, base);
+            send(k2 + 1, base + 16384);
+            bulk_commit();
+          }
+        };
 #pragma unroll
         for (int k2 = 0; k2 < D / 32; k2 += 2) {
           load_pair(k2);
@@ -664,22 +679,15 @@ __device__ void bwd_drain(const BwdArgs& a, const CUtensorMap* dq_map, const CUt
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.dq_empty));
           }
+          if constexpr (D == 128 && !kPack) {
+            if (whole && k2 > 0) send_half(k2 - 2, do_box);
+          }
           const uint32_t base = k2 < kHalf ? do_box + k2 * 16384 : ds_box + (k2 - kHalf) * 16384;
           put(k2, base, vv[0]);
           put(k2 + 1, kHalf == 1 ? ds_box : base + 16384, vv[1]);
-          if constexpr (D == 128 && !kPack) {
-            // one pair = one half: group 1 (the dO-half boxes) leaves while the
-            // second pair is read, group 2 (the dS^T-buffer boxes) after it
-            if (whole) {
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                send(k2, base);
-                send(k2 + 1, base + 16384);
-                bulk_commit();
-              }
-            }
-          }
+        }
+        if constexpr (D == 128 && !kPack) {
+          if (whole) send_half(D / 32 - 2, ds_box);
         }
         if constexpr (D != 128 || kPack) {
           if (whole) fence_proxy_async_smem();
