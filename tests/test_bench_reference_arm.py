@@ -24,3 +24,18 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_stored_traffic_matches_the_current_kernel_sources():
+    # bench.py reports roofline.traffic only while the stored ncu counters were
+    # taken from the sources that are built now; every entry must name a kernel
+    # of this library and carry the hash of its current source file and headers
+    import bench
+    src = {"jfa_fwd_kernel": "fwd.cu", "jfa_fwd2_kernel": "fwd2.cu", "jfa_bwd_kernel": "bwd.cu"}
+    assert bench.NCU_TRAFFIC
+    for key, entry in bench.NCU_TRAFFIC.items():
+        kernel, workload = key.split(":")[:2]
+        assert kernel in src and workload in bench.workloads.WORKLOADS, key
+        assert entry["bytes"] > 0
+        assert entry["src_hash"] == bench.src_hash(src[kernel]), (
+            f"{key}: counters taken from other sources; re-capture them (profiles/ gives the command)")
