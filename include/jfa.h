@@ -231,6 +231,18 @@ int jfa_build_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_hos
                     int32_t* cta_ptr_out, int* T, int* P);
 
 /*
+ * Host-only (no GPU needed): the schedule choices jfa_plan_create_ex makes
+ * for these arguments on a device of num_ctas SMs (num_ctas >= 1 here):
+ * *fwd_form as jfa_plan_forward_form, *fwd_claims / *bwd_claims as
+ * jfa_plan_claims, *packed = 1 when short sequences are packed into shared
+ * tiles (JFA_PLAN_PACK_SHORT's rule).  Any output pointer may be NULL.
+ * Errors as jfa_plan_create_ex (offsets, sizes, conflicting flags).
+ */
+int jfa_plan_choices(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                     int Lq, int D, int num_ctas, unsigned flags, int* fwd_form, int* fwd_claims,
+                     int* bwd_claims, int* packed);
+
+/*
  * Host-only (no GPU needed): *in_tiles = 1 when a plan created from these
  * offsets and flags has its backward tiles form Delta (the rule given with
  * JFA_PLAN_DELTA_PREPASS), 0 when the pre-pass forms it.  With 1, jfa_bwd

@@ -194,6 +194,25 @@ def delta_in_tiles(kv_offsets, q_offsets=None, *, Lq: int = 0, flags: int = 0) -
     return bool(res.value)
 
 
+def plan_choices(kv_offsets, q_offsets=None, *, H: int, D: int, Lq: int = 0, num_ctas: int,
+                 flags: int = 0) -> dict:
+    """Host-only (no GPU): the schedule choices a plan with these arguments makes
+    on a device of ``num_ctas`` SMs (jfa_plan_choices): ``forward_form`` (0 one
+    query tile per CTA, 1 CTA pairs, 2 two query tiles per CTA), whether the
+    forward / backward claim their tiles at run time, and whether short
+    sequences are packed."""
+    kv = _offsets(kv_offsets)
+    qo = _offsets(q_offsets)
+    fn = lib().jfa_plan_choices
+    fn.argtypes = [_i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_uint, _ip, _ip, _ip, _ip]
+    fn.restype = ctypes.c_int
+    form, fc, bc, pk = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(fn(_i32ptr(kv), _i32ptr(qo), kv.size - 1, H, Lq, D, num_ctas, flags, ctypes.byref(form),
+              ctypes.byref(fc), ctypes.byref(bc), ctypes.byref(pk)), "jfa_plan_choices")
+    return {"forward_form": form.value, "claims": (bool(fc.value), bool(bc.value)), "packed": bool(pk.value)}
+
+
 class Plan:
     """A jfa_plan_t: offsets and tile schedules resident on the current device."""
 

@@ -224,6 +224,23 @@ bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, in
   return true;
 }
 
+// The schedule choices a plan makes from its sizes, offsets and flags (plan
+// creation and the host-only jfa_plan_choices share this).
+struct PlanChoices {
+  bool packed = false, fwd_dynamic = false, bwd_dynamic = false, fwd_pair = false, fwd_two = false;
+  std::vector<int> pack;
+};
+PlanChoices choose(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B, int H, int D,
+                   int num_ctas, const std::vector<int64_t>& qlen, const std::vector<int64_t>& kvlen) {
+  PlanChoices c;
+  c.packed = use_packing(flags, kv_off, q_off, B, kvlen, &c.pack);
+  c.fwd_dynamic = claims_fwd(flags);
+  c.bwd_dynamic = claims_bwd(flags, q_off == nullptr);
+  c.fwd_pair = use_fwd_pairs(flags, D, c.packed, c.fwd_dynamic, num_ctas, qlen);
+  c.fwd_two = !c.fwd_pair && use_fwd_two(flags, D, H, c.packed, c.fwd_dynamic, num_ctas, qlen, kvlen);
+  return c;
+}
+
 }  // namespace
 
 extern "C" {
@@ -283,6 +300,25 @@ int jfa_delta_in_tiles(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   return JFA_OK;
 }
 
+int jfa_plan_choices(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
+                     int Lq, int D, int num_ctas, unsigned flags, int* fwd_form, int* fwd_claims,
+                     int* bwd_claims, int* packed) {
+  if (!kv_offsets_host || B < 1 || H < 1 || num_ctas < 1) return JFA_ERR_INVALID_ARG;
+  if ((flags & JFA_PLAN_DELTA_PREPASS) && (flags & JFA_PLAN_DELTA_IN_TILES)) return JFA_ERR_INVALID_ARG;
+  if (bad_flags(flags)) return JFA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+  std::vector<int64_t> qlen, kvlen;
+  int64_t n_kv = 0, n_q = 0;
+  int rc = lengths_of(kv_offsets_host, q_offsets_host, B, Lq, qlen, kvlen, &n_kv, &n_q);
+  if (rc != JFA_OK) return rc;
+  const PlanChoices ch = choose(flags, kv_offsets_host, q_offsets_host, B, H, D, num_ctas, qlen, kvlen);
+  if (fwd_form) *fwd_form = ch.fwd_pair ? 1 : ch.fwd_two ? 2 : 0;
+  if (fwd_claims) *fwd_claims = ch.fwd_dynamic ? 1 : 0;
+  if (bwd_claims) *bwd_claims = ch.bwd_dynamic ? 1 : 0;
+  if (packed) *packed = ch.packed ? 1 : 0;
+  return JFA_OK;
+}
+
 int jfa_plan_create(const int32_t* kv_offsets_host, const int32_t* q_offsets_host, int B, int H,
                     int Lq, int D, int num_ctas, void* stream, jfa_plan_t* out) {
   return jfa_plan_create_ex(kv_offsets_host, q_offsets_host, B, H, Lq, D, num_ctas, 0u, stream, out);
@@ -322,8 +358,9 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
   p->n_q = n_q;
   p->n_o = n_o;
   p->n_kv = n_kv;
-  std::vector<int> pack;
-  p->packed = use_packing(flags, kv_offsets_host, q_offsets_host, B, kvlen, &pack);
+  const PlanChoices ch = choose(flags, kv_offsets_host, q_offsets_host, B, H, D, p->num_ctas, qlen, kvlen);
+  const std::vector<int>& pack = ch.pack;
+  p->packed = ch.packed;
   if (!q_offsets_host) {
     if (n_q > 0) p->dq_rows_to_clear.emplace_back(0, n_q);
   } else {
@@ -348,10 +385,10 @@ int jfa_plan_create_ex(const int32_t* kv_offsets_host, const int32_t* q_offsets_
       p->dq_own_rows = true;
     }
   }
-  p->fwd_dynamic = claims_fwd(flags);
-  p->bwd_dynamic = claims_bwd(flags, p->broadcast);
-  p->fwd_pair = use_fwd_pairs(flags, D, p->packed, p->fwd_dynamic, p->num_ctas, qlen);
-  p->fwd_two = !p->fwd_pair && use_fwd_two(flags, D, H, p->packed, p->fwd_dynamic, p->num_ctas, qlen, kvlen);
+  p->fwd_dynamic = ch.fwd_dynamic;
+  p->bwd_dynamic = ch.bwd_dynamic;
+  p->fwd_pair = ch.fwd_pair;
+  p->fwd_two = ch.fwd_two;
   p->fwd = p->fwd_pair  ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas / 2, nullptr, false)
            : p->fwd_two ? jfa::build_fwd_schedule(pair_lengths(qlen), kvlen, H, p->num_ctas, nullptr, false)
                         : jfa::build_fwd_schedule(qlen, kvlen, H, p->num_ctas, p->packed ? &pack : nullptr,

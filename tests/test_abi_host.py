@@ -409,3 +409,58 @@ def test_native_builder_cost_order_both_sort_paths(lengths):
             rt, rp = ref_tiles.fwd_tiles(np.full(len(kl), 1000), kl, 3, 128, 128, 7, None, dyn) if d == 0 \
                 else ref_tiles.bwd_tiles(np.full(len(kl), 1000), kl, 3, 128, 128, 7, None, dyn)
             assert np.array_equal(t, rt) and np.array_equal(p, rp)
+
+
+def _choices(kv_lengths, q_lengths=None, *, H=4, D=128, Lq=0, num_ctas=16, flags=0):
+    kv = np.concatenate([[0], np.cumsum(kv_lengths)]).astype(np.int32)
+    qo = None if q_lengths is None else np.concatenate([[0], np.cumsum(q_lengths)]).astype(np.int32)
+    return jfa.plan_choices(kv, qo, H=H, D=D, Lq=Lq, num_ctas=num_ctas, flags=flags)
+
+
+def test_two_tile_forward_rule_at_its_thresholds():
+    # two query tiles per CTA where the tiles of two query blocks hold >= 3 key
+    # blocks on average, at most a quarter of them hold one query block, and
+    # there are at least four of them per CTA (counted over heads)
+    assert _choices([384] * 16, Lq=256)["forward_form"] == 2          # 3 key blocks, 64 tiles / 16 CTAs
+    assert _choices([256] * 16, Lq=256)["forward_form"] == 0          # 2 key blocks
+    assert _choices([384] * 16, Lq=256, num_ctas=17)["forward_form"] == 0   # under four per CTA
+    assert _choices([384] * 16, Lq=384)["forward_form"] == 0          # half of the tiles half empty
+    assert _choices([384] * 16, Lq=1152)["forward_form"] == 2         # one in five half empty
+    assert _choices([384] * 16, Lq=640)["forward_form"] == 0          # one in three
+    assert _choices([384] * 16, Lq=256, D=64)["forward_form"] == 0    # D = 128 only
+    # the flags force either way, within what the kernels support
+    assert _choices([256] * 16, Lq=256, flags=jfa.PLAN_FWD_TWO)["forward_form"] == 2
+    assert _choices([384] * 16, Lq=256, flags=jfa.PLAN_FWD_ONE)["forward_form"] == 0
+    assert _choices([384] * 16, Lq=256, flags=jfa.PLAN_FWD_PAIRS)["forward_form"] == 1
+    assert _choices([384] * 16, Lq=256, flags=jfa.PLAN_FWD_TWO | jfa.PLAN_DYNAMIC)["forward_form"] == 0
+    assert _choices([384] * 16, Lq=256, D=64, flags=jfa.PLAN_FWD_TWO)["forward_form"] == 0
+
+
+def test_claim_and_packing_rules():
+    # the backward claims its tiles at run time in self mode; both passes with
+    # JFA_PLAN_DYNAMIC, neither with JFA_PLAN_STATIC
+    assert _choices([300, 500], Lq=256)["claims"] == (False, False)
+    assert _choices([300, 500], [300, 500])["claims"] == (False, True)
+    assert _choices([300, 500], Lq=256, flags=jfa.PLAN_DYNAMIC)["claims"] == (True, True)
+    assert _choices([300, 500], [300, 500], flags=jfa.PLAN_STATIC)["claims"] == (False, False)
+    # short self-mode sequences are packed when that removes an eighth of the
+    # forward tiles; never in broadcast mode or with JFA_PLAN_NO_PACK
+    assert _choices([64] * 32, [64] * 32)["packed"]
+    assert not _choices([64] * 32, [64] * 32, flags=jfa.PLAN_NO_PACK)["packed"]
+    assert not _choices([64] * 32, Lq=64)["packed"]
+    assert not _choices([1024] * 32, [1024] * 32)["packed"]
+
+
+def test_plan_choices_rejects_bad_arguments():
+    L = jfa.lib()
+    kv = np.array([0, 4, 6], dtype=np.int32)
+    out = ctypes.c_int()
+    p = kv.ctypes.data_as(jfa._i32p)
+    assert L.jfa_plan_choices(p, None, 2, 1, 4, 128, 0, 0, ctypes.byref(out), None, None, None) == 1
+    assert L.jfa_plan_choices(None, None, 2, 1, 4, 128, 8, 0, None, None, None, None) == 1
+    assert L.jfa_plan_choices(p, None, 2, 1, 4, 96, 8, 0, None, None, None, None) == 2   # D
+    assert L.jfa_plan_choices(p, None, 2, 1, 4, 128, 8,
+                              jfa.PLAN_FWD_TWO | jfa.PLAN_FWD_ONE, None, None, None, None) == 1
+    bad = np.array([0, 6, 4], dtype=np.int32)
+    assert L.jfa_plan_choices(bad.ctypes.data_as(jfa._i32p), None, 2, 1, 4, 128, 8, 0,
+                              None, None, None, None) == 3
