@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -43,10 +44,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum of a
 # 256-sequence capture of the same kernel, scaled by K/V tokens: x3.730),
-# keyed by kernel and workload, valid only while the kernel source hash matches.
+# keyed by kernel and workload, valid only while the hash of the code the
+# kernel compiles from (comments aside) matches.
 NCU_TRAFFIC = {
-    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2421e+09, "src_hash": "df55b77c5dfbab62"},
-    "jfa_fwd2_kernel:gem_broadcast": {"bytes": 1.7841e+09, "src_hash": "6d874a31595e22c6"},
+    "jfa_bwd_kernel:gem_broadcast": {"bytes": 3.2421e+09, "src_hash": "ec96008415c21b59"},
+    "jfa_fwd2_kernel:gem_broadcast": {"bytes": 1.7841e+09, "src_hash": "f7fdb3ba4f8766af"},
 }
 
 
@@ -191,13 +193,25 @@ def alg_bytes(prob, which: str, pack: bool = False, own_delta: bool = False) -> 
     return q + 2 * kv + o + (1 if own_delta else 2) * lse + prob.n_q_rows * row * 4 + 2 * kv
 
 
+_COMMENT_OR_STRING = re.compile(r'"(?:\\.|[^"\\\n])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def code_text(text: str) -> str:
+    """C/CUDA source with its comments removed and whitespace runs collapsed
+    (string literals kept as written): what the compiler sees."""
+    code = _COMMENT_OR_STRING.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return " ".join(code.split())
+
+
 def src_hash(name: str) -> str:
-    """Hash of a kernel's source file and the local headers it includes, so that
-    stored ncu traffic goes stale whenever any code the kernel compiles from changes."""
+    """Hash of the code (not the comments) of a kernel's source file and the
+    local headers it includes, so that stored ncu traffic goes stale whenever
+    any code the kernel compiles from changes."""
     csrc = ROOT / "jagged_attention_gb300" / "csrc"
     h = hashlib.sha256()
     for f in (name, "kernels.h", "sm103_ptx.cuh", "tiles.cuh"):
-        h.update((csrc / f).read_bytes())
+        h.update(code_text((csrc / f).read_text()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

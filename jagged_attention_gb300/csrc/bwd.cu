@@ -97,7 +97,7 @@ struct BwdCfg {
   static constexpr int kOffQ = 2 * kTileBytes;        // 2 stages
   static constexpr int kOffDO = 4 * kTileBytes;       // 2 stages
   static constexpr int kOffDS = 6 * kTileBytes;       // dS^T [128 keys x 128 queries] bf16
-  static constexpr int kOffLse = kOffDS + 32768;      // 128 -LSE*log2(e), 128 Delta (fp32)
+  static constexpr int kOffLse = kOffDS + 32768;      // 128 -LSE*log2(e), 128 -scale*Delta (fp32)
   static constexpr int kOffBar = kOffLse + 1024;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;

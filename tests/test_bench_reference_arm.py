@@ -39,3 +39,14 @@ def test_stored_traffic_matches_the_current_kernel_sources():
         assert entry["bytes"] > 0
         assert entry["src_hash"] == bench.src_hash(src[kernel]), (
             f"{key}: counters taken from other sources; re-capture them (profiles/ gives the command)")
+
+
+def test_source_hash_follows_code_not_comments():
+    # a comment or a re-wrap leaves the code text (and so the hash) unchanged;
+    # any change to code, string literals included, changes it
+    import bench
+    src = 'int a = 1;  // one\n/* two\n   lines */ asm("add.s32 %0, %1; // kept");\n'
+    same = 'int a = 1;\n// another comment\nasm("add.s32 %0, %1; // kept"); /* x */\n'
+    assert bench.code_text(src) == bench.code_text(same)
+    assert bench.code_text(src) != bench.code_text(src.replace("a = 1", "a = 2"))
+    assert bench.code_text(src) != bench.code_text(src.replace("// kept", "// gone"))
