@@ -75,9 +75,9 @@ __global__ void __launch_bounds__(256)
 // staging -> tensor reduce-add into the fp32 dq (in broadcast mode every
 // sequence's tiles add into the same rows: the cross-batch reduction of the
 // GEM page, "GEM's sequences do not fit a fixed grid").  The TMEM slice
-// holding dQ_m is released as soon as it sits in shared memory (the pages'
-// early TMEM release).  At the end of a tile the same group writes dV and
-// scale*dK in bf16.
+// holding dQ_m is released as soon as all of it is in registers, before its
+// last columns are staged (the pages' early TMEM release).  At the end of a
+// tile the same group writes dV and scale*dK in bf16.
 //
 //   warps 0-7   two softmax groups: P^T and dS^T (thread = key row), query
 //               columns split in halves
@@ -249,7 +249,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, BwdBars
         mma_bf16_ss(tmem + C::kColS, desc_at(kd_k, koff), desc_at(qd_k, koff), id_sdp, kk > 0 ? 1u : 0u);
       }
       mma_commit(smem_u32(&bars.s_full));
-      // dP^T region is free once WG1 has the previous dQ in registers
+      // dP^T region is free once the drain group has the previous dQ in registers
       ok = mbar_wait(smem_u32(&bars.dq_empty), (gm & 1) ^ 1, ab);
       if (ok && m == 0) ok = mbar_wait(smem_u32(&bars.kv_full[vb]), tt & 1, ab);
       if (!ok) break;
@@ -330,7 +330,7 @@ __device__ __forceinline__ void bwd_softmax_loop(const BwdArgs& a, uint8_t* smem
   const int r = (warp & 3) * 32 + lane;  // key row of the tile = TMEM lane
   const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int c0 = 64 * g;                 // first query column of this group
-  float* lse2 = reinterpret_cast<float*>(smem + C::kOffLse);  // 128 -LSE*log2(e), then 128 Delta
+  float* lse2 = reinterpret_cast<float*>(smem + C::kOffLse);  // 128 -LSE*log2(e), then 128 -scale*Delta
   float* dlt = lse2 + 128;
   const uint32_t lse_ready = smem_u32(&bars.lse_ready[g]), lse_done = smem_u32(&bars.lse_done[g]);
   uint32_t gm = 0, tt = 0;
@@ -521,9 +521,9 @@ __device__ void bwd_softmax(const BwdArgs& a, uint8_t* smem, uint32_t sbase, uin
 
 // ---------------------------------------------------------------------------
 // Drain group (warps 10-13): dQ_m leaves TMEM (thread = query row), the TMEM
-// columns are released as soon as it is in shared memory, and tensor reduce-adds
-// into dq follow (the cross-batch reduction of the broadcast mode happens
-// here, in the memory system).  At the end of a tile the group also writes dV
+// columns are released as soon as all of it is in registers, and tensor
+// reduce-adds into dq follow each staged pair of boxes (the cross-batch
+// reduction of the broadcast mode happens here, in the memory system).  At the end of a tile the group also writes dV
 // and scale * dK (thread = key row) as bf16 boxes of 32 x 64.
 // Whether key row r of tile t belongs to the tile's sequence(s).
 template <bool kPack>

@@ -357,7 +357,7 @@ __device__ void fwd_pair_forwarder(const FwdArgs& a, FwdBars& bars, const Abort&
 }
 
 // ---------------------------------------------------------------------------
-// softmax / correction / epilogue (warps 0-3, thread = query row = TMEM lane)
+// softmax / correction / epilogue (warps 0-7 in two groups, thread = query row = TMEM lane)
 // ---------------------------------------------------------------------------
 template <int D, bool kPack, bool kPair, class Seq>
 __device__ void fwd_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t* smem, uint32_t tmem,

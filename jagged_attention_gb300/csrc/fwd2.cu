@@ -394,7 +394,7 @@ __device__ void fwd2_softmax(const FwdArgs& a, const CUtensorMap* o_map, uint8_t
       const float inv_l = 1.0f / lr_all;
       const int64_t orow = o_base + X * 128 + r;
       // a warp whose 32 rows all belong to the sequence stores them as one
-      // swizzled box through the Q buffer; others store their valid rows
+      // swizzled box through that stage; others store their valid rows
       const bool staged = __all_sync(0xffffffffu, row_ok[X]);
       const uint32_t stg = smem_u32(smem + (X == 0 ? C::kOffK : C::kOffV) + sl * C::kTileBytes) +
                            grp * C::kChunkBytes + wq * 4096;
