@@ -29,7 +29,10 @@
  *
  * Ownership: the caller owns every tensor and the stream.  A plan owns a
  * small device copy of the offsets and of the tile schedule; it must outlive
- * the stream work that uses it.  jfa_fwd / jfa_bwd allocate nothing and are
+ * the stream work that uses it.  A plan belongs to the device that was
+ * current when it was created: jfa_fwd, jfa_bwd (and its stages) and
+ * jfa_plan_device_status return JFA_ERR_INVALID_ARG when another device is
+ * current.  jfa_fwd / jfa_bwd allocate nothing and are
  * asynchronous on the given stream (a cudaStream_t passed as void*; NULL is
  * the legacy default stream).
  *

@@ -87,6 +87,14 @@ jfa::Problem problem_of(const jfa_plan* p) {
   return pb;
 }
 
+// A plan's device block and launches belong to the device that was current
+// when it was created; calls that use them must run with that device current.
+int check_device(const jfa_plan* p) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_CUDA;
+  return dev == p->device ? JFA_OK : JFA_ERR_INVALID_ARG;
+}
+
 // Lengths from host offsets; q_off == nullptr means broadcast with Lq rows.
 int lengths_of(const int32_t* kv_off, const int32_t* q_off, int B, int Lq,
                std::vector<int64_t>& qlen, std::vector<int64_t>& kvlen, int64_t* n_kv,
@@ -144,12 +152,6 @@ bool tiles_form_delta(unsigned flags, const std::vector<int64_t>& qlen,
   return (flags & JFA_PLAN_DELTA_IN_TILES) || mean_tile_keys(bwd, kv_off) >= 96.0;
 }
 
-// Whether the plan packs short sequences, and the packing (pack[b] as
-// short_packs gives it) when it does.  Packing needs self mode with one
-// offsets array for queries and keys.  JFA_PLAN_PACK_SHORT packs whenever a
-// run forms, JFA_PLAN_NO_PACK never; by default a plan packs when that
-// removes at least an eighth of its forward tiles (a pack of n non-empty
-// sequences replaces n one-block tiles by one).
 // Whether the forward runs as CTA pairs (two CTAs of a cluster take the two
 // query blocks of a pair tile and share each K/V block, the tensor-core
 // products spanning both: cta_group::2): on request, where the pair kernel
@@ -205,6 +207,12 @@ bool use_fwd_two(unsigned flags, int D, int H, bool packed, bool dynamic, int nu
   return blocks >= 3 * tiles && 4 * half <= tiles && tiles * H >= 4 * int64_t(num_ctas);
 }
 
+// Whether the plan packs short sequences, and the packing (pack[b] as
+// short_packs gives it) when it does.  Packing needs self mode with one
+// offsets array for queries and keys.  JFA_PLAN_PACK_SHORT packs whenever a
+// run forms, JFA_PLAN_NO_PACK never; by default a plan packs when that
+// removes at least an eighth of its forward tiles (a pack of n non-empty
+// sequences replaces n one-block tiles by one).
 bool use_packing(unsigned flags, const int32_t* kv_off, const int32_t* q_off, int B,
                  const std::vector<int64_t>& kvlen, std::vector<int>* pack) {
   if ((flags & JFA_PLAN_NO_PACK) || !q_off) return false;
@@ -494,6 +502,7 @@ int jfa_plan_tiles(jfa_plan_t plan, int dir, int32_t* tiles_host, int32_t* cta_p
 
 int jfa_plan_device_status(jfa_plan_t plan, void* stream, int* raw) {
   if (!plan) return JFA_ERR_INVALID_ARG;
+  if (int rc = check_device(plan)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int word = 0;
   if (cudaMemcpyAsync(&word, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -510,6 +519,7 @@ int jfa_plan_device_status(jfa_plan_t plan, void* stream, int* raw) {
 int jfa_fwd(jfa_plan_t plan, const void* q, const void* k, const void* v, float scale, void* out,
             float* lse, void* stream) {
   if (!plan || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if (int rc = check_device(plan)) return rc;
   if ((plan->n_q > 0 && !q) || (plan->n_kv > 0 && (!k || !v)) || (plan->n_o > 0 && (!out || !lse)))
     return JFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
@@ -554,6 +564,7 @@ size_t jfa_bwd_workspace_bytes(jfa_plan_t plan) {
 int jfa_bwd_preprocess(jfa_plan_t plan, const void* out, const void* dout, float* dq, void* dk,
                        void* dv, void* workspace, size_t workspace_bytes, void* stream) {
   if (!plan) return JFA_ERR_INVALID_ARG;
+  if (int rc = check_device(plan)) return rc;
   if ((plan->n_q > 0 && !dq) || (plan->n_kv > 0 && (!dk || !dv)) ||
       (plan->n_o > 0 && (!out || !dout)))
     return JFA_ERR_INVALID_ARG;
@@ -591,6 +602,7 @@ int jfa_bwd_main(jfa_plan_t plan, const void* q, const void* k, const void* v, c
                  const float* lse, float scale, float* dq, void* dk, void* dv,
                  const void* workspace, size_t workspace_bytes, void* stream) {
   if (!plan || !std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+  if (int rc = check_device(plan)) return rc;
   if ((plan->n_q > 0 && (!q || !dq)) || (plan->n_kv > 0 && (!k || !v || !dk || !dv)) ||
       (plan->n_o > 0 && (!dout || !lse)))
     return JFA_ERR_INVALID_ARG;
