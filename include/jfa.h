@@ -436,9 +436,9 @@ int jfa_bwd_simple(const void* q, const void* k, const void* v, const int32_t* k
                    const void* out, const void* dout, const float* lse, float* dq, void* dk,
                    void* dv, void* stream);
 
-/* Device status of every cached plan (synchronises `stream`, then clears the
- * words): JFA_ERR_DEVICE_TIMEOUT when any recorded a wait that ran out;
- * *raw (optional) receives the words or-ed together. */
+/* Device status of every cached plan of the current device (synchronises
+ * `stream`, then clears the words): JFA_ERR_DEVICE_TIMEOUT when any recorded
+ * a wait that ran out; *raw (optional) receives the words or-ed together. */
 int jfa_simple_device_status(void* stream, int* raw);
 
 /* Release every cached plan and workspace (synchronises the device). */
