@@ -913,7 +913,7 @@ extern "C" int jfa_bwd_simple(const void* q, const void* k, const void* v,
 extern "C" int jfa_simple_device_status(void* stream, int* raw) {
   std::lock_guard<std::mutex> lock(g_simple_mu);
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_CUDA;
+  if (!g_simple.empty() && cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_CUDA;
   int word = 0, rc = JFA_OK;
   for (auto& e : g_simple) {
     if (e.device != dev) continue;  // read with that device current
