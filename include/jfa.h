@@ -334,11 +334,11 @@ int jfa_plan_device_status(jfa_plan_t plan, void* stream, int* raw);
  * memory and calls no allocating library routine.  It uploads the schedule
  * and offsets with cudaMemcpyAsync from a host buffer that lives only for
  * the call (pageable memory), so the call returns once that copy has been
- * taken from the host buffer.
+ * taken from the host buffer, and the call cannot be captured into a CUDA
+ * graph (a replay would read that buffer after the call has returned).
  *
  * The first call on a device resolves the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array and each call
+ * (cudaGetSymbolAddress, with that device current).  All calls share the one array and each call
  * rewrites what it needs (nothing is assumed to start at zero), so calls
  * that overlap on the GPU -- different streams, or different host threads
  * without ordering -- race; issue them on one stream or order them.
