@@ -4,8 +4,9 @@ share every K/V block, and the CTA alternates between them.  Checked against
 the fp64 oracle, and against the one-tile forward on the same inputs, on
 broadcast and self-mode batches: empty sequences, ragged key tails, a tile
 whose second query block is empty or partial, few CTAs for many tiles (each
-tile's O leaving through its Q buffers while the next tile waits for them),
-the backward after it, and when a plan runs it."""
+tile's O leaving through the K and V stages of its last key block while the
+producer's next loads into those stages wait for it), the backward after it,
+and when a plan runs it."""
 import numpy as np
 import pytest
 import torch
