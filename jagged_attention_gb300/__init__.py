@@ -214,7 +214,8 @@ def plan_choices(kv_offsets, q_offsets=None, *, H: int, D: int, Lq: int = 0, num
 
 
 class Plan:
-    """A jfa_plan_t: offsets and tile schedules resident on the current device."""
+    """A jfa_plan_t: offsets and tile schedules resident on the current device,
+    which must be current again whenever the plan is used."""
 
     def __init__(self, kv_offsets, q_offsets=None, *, H: int, D: int, Lq: int = 0,
                  num_ctas: int = 0, flags: int = 0, stream=None):
